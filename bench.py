@@ -1,0 +1,502 @@
+"""Benchmark of the SWA(w, s) hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of the Llama-3.1-8B
+shaped single-layer workload (B=1, L=4096, Hq=32, Hkv=8, d=128, SWA(w=128,
+s=4), bf16, q/k/v ~ N(0,1) with the four sink keys scaled x4):
+    swa_prefill  ->  swa_cache_append (prompt survivors)
+                 ->  swa_cache_append (one new token)  ->  swa_decode (pos = L)
+Metric: in-band TFLOP/s = 4 * B * Hq * d * (sum over the step's query rows of
+|K(t)|) / step time. The decode half of the metric (KV GB/s at batch 64, 68-slot
+cache, SWA(64, 4)) is measured in the same run and reported under "decode".
+
+Steps rotate over input sets whose total exceeds the 126 MB L2, each set
+replayed as one CUDA graph of the step. Timing uses CUDA events on the
+launching stream. Under torchrun each rank runs an independent replica on its
+own GPU (no data-path collective); the time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import swa_inputs  # noqa: E402
+
+WORKLOAD = dict(name="llama3.1-8b-layer-prefill+decode SWA(128,4)", B=1, L=4096, Hq=32, Hkv=8,
+                d=128, w=128, s=4, sink_rows=4, seed=1002)
+DECODE = dict(name="decode SWA(64,4) batch 64, 68-slot ring cache", B=64, Hq=32, Hkv=8, d=128,
+              w=64, s=4, pos=262143)
+L2_BYTES = 126 * 1024 * 1024
+
+
+def pairs_per_head(L: int, w: int, s: int) -> int:
+    """sum over t < L of |K(t)| = min(t+1, w) + min(s, max(0, t-w+1))."""
+    t = np.arange(L, dtype=np.int64)
+    return int(np.sum(np.minimum(t + 1, w) + np.minimum(s, np.maximum(0, t - w + 1))))
+
+
+def keys_of_row(t: int, w: int, s: int) -> int:
+    return min(t + 1, w) + min(s, max(0, t - w + 1))
+
+
+def step_flops(cfg) -> float:
+    rows = pairs_per_head(cfg["L"], cfg["w"], cfg["s"]) + keys_of_row(cfg["L"], cfg["w"], cfg["s"])
+    return 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * rows
+
+
+def prefill_bytes(cfg) -> int:
+    """Algorithmic bytes of one prefill launch: Q, K, V read once, O written once."""
+    return cfg["B"] * cfg["L"] * (2 * cfg["Hq"] + 2 * cfg["Hkv"]) * cfg["d"] * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str | None = None):
+        self.gpu_index = gpu_index
+        self.path = path
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if self.path:
+                with open(self.path, "w") as f:
+                    f.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        loaded = [x for x in sm if x > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def make_step_inputs(cfg, n_sets, device, seed_offset=0):
+    sets = []
+    for i in range(n_sets):
+        q, k, v = swa_inputs.prefill_inputs(cfg["B"], cfg["L"], cfg["Hq"], cfg["Hkv"], cfg["d"],
+                                            cfg["seed"] + seed_offset + 97 * i,
+                                            sink_rows=cfg["sink_rows"])
+        g = torch.Generator("cpu").manual_seed(cfg["seed"] + 7 + 97 * i)
+        qn = torch.randn(cfg["B"], cfg["Hq"], cfg["d"], generator=g).to(torch.bfloat16)
+        kn = torch.randn(cfg["B"], 1, cfg["Hkv"], cfg["d"], generator=g).to(torch.bfloat16)
+        vn = torch.randn(cfg["B"], 1, cfg["Hkv"], cfg["d"], generator=g).to(torch.bfloat16)
+        sets.append(dict(q=q, k=k, v=v, qn=qn, kn=kn, vn=vn))
+    return sets
+
+
+class GpuStep:
+    """Device-resident buffers of one input set and the hot-path calls."""
+
+    def __init__(self, swa, cfg, host, device):
+        self.swa, self.cfg = swa, cfg
+        B, L, Hq, Hkv, d, w, s = (cfg[x] for x in ("B", "L", "Hq", "Hkv", "d", "w", "s"))
+        self.dev = {k: t.to(device) for k, t in host.items()}
+        self.out = torch.empty(B, L, Hq, d, dtype=torch.bfloat16, device=device)
+        self.kc = torch.zeros(B, Hkv, s + w, d, dtype=torch.bfloat16, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        self.pos0 = torch.zeros(B, dtype=torch.int32, device=device)
+        self.posL = torch.full((B,), L, dtype=torch.int32, device=device)
+        self.dec = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=device)
+        need = swa.swa_decode_workspace_size(B, Hq, Hkv, d, w, s)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device) if need else None
+        self.graph_prefill = None
+        self.graph_rest = None
+
+    def prefill(self):
+        c = self.cfg
+        self.swa.swa_prefill(self.dev["q"], self.dev["k"], self.dev["v"], c["w"], c["s"],
+                             out=self.out)
+
+    def rest(self):
+        c = self.cfg
+        self.swa.swa_cache_append(self.dev["k"], self.dev["v"], self.kc, self.vc, self.pos0,
+                                  c["w"], c["s"])
+        self.swa.swa_cache_append(self.dev["kn"], self.dev["vn"], self.kc, self.vc, self.posL,
+                                  c["w"], c["s"])
+        self.swa.swa_decode(self.dev["qn"], self.kc, self.vc, self.posL, c["w"], c["s"],
+                            out=self.dec, workspace=self.ws)
+
+    def capture(self, stream):
+        self.graph_prefill = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_prefill, stream=stream):
+            self.prefill()
+        self.graph_rest = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_rest, stream=stream):
+            self.rest()
+
+
+def launches_per_step(swa, cfg) -> int:
+    splits_ws = swa.swa_decode_workspace_size(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["w"],
+                                              cfg["s"])
+    return 1 + 2 + (2 if splits_ws else 1)
+
+
+def bench_decode(swa, device, stream, iters=64, warmup=8):
+    """Kernel-only decode at batch 64 over a rotating pool of distinct caches
+    (> 4x L2), replayed as one CUDA graph of `ncache` decode launches."""
+    c = DECODE
+    B, Hq, Hkv, d, w, s = (c[x] for x in ("B", "Hq", "Hkv", "d", "w", "s"))
+    kv_bytes = B * Hkv * (s + w) * d * 2 * 2
+    ncache = max(8, int(math.ceil(4 * L2_BYTES / kv_bytes)))
+    g = torch.Generator(device=device).manual_seed(1003)
+    caches = [(torch.randn(B, Hkv, s + w, d, generator=g, device=device).to(torch.bfloat16),
+               torch.randn(B, Hkv, s + w, d, generator=g, device=device).to(torch.bfloat16))
+              for _ in range(ncache)]
+    q = torch.randn(B, Hq, d, generator=g, device=device).to(torch.bfloat16)
+    pos = torch.full((B,), c["pos"], dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+    with torch.cuda.stream(stream):
+        for kc, vc in caches[:2]:
+            swa.swa_decode(q, kc, vc, pos, w, s, out=out)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for kc, vc in caches:
+                swa.swa_decode(q, kc, vc, pos, w, s, out=out)
+        for _ in range(warmup):
+            graph.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms_per_launch = e0.elapsed_time(e1) / (iters * ncache)
+    gbs = kv_bytes / (ms_per_launch * 1e-3) / 1e9
+    return dict(kv_bytes_per_launch=kv_bytes, us_per_launch=ms_per_launch * 1e3, gbs=gbs,
+                caches=ncache, pool_bytes=ncache * kv_bytes)
+
+
+def run_gpu(args):
+    import sliding_window_attention_05_b300 as swa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device)
+    cfg = WORKLOAD
+    peaks = load_peaks()
+
+    set_bytes = prefill_bytes(cfg)
+    n_sets = max(2, int(math.ceil(2.5 * L2_BYTES / set_bytes)))
+    host_sets = make_step_inputs(cfg, n_sets, device, seed_offset=1000 * rank)
+    steps = [GpuStep(swa, cfg, h, device) for h in host_sets]
+    with torch.cuda.stream(stream):
+        for st in steps:           # eager warm-up (first-call setup happens here)
+            st.prefill()
+            st.rest()
+        stream.synchronize()
+        for st in steps:
+            st.capture(stream)
+        for i in range(args.warmup):
+            st = steps[i % n_sets]
+            st.graph_prefill.replay()
+            st.graph_rest.replay()
+        stream.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local, clocks_path) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(K):
+                st = steps[i % n_sets]
+                ev[i][0].record(stream)
+                st.graph_prefill.replay()
+                ev[i][1].record(stream)
+                st.graph_rest.replay()
+            end.record(stream)
+        torch.cuda.synchronize(device)
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    prefill_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    total_ms = max_over_ranks(total_ms, world, device)
+    ms_per_step = total_ms / K
+    value = step_flops(cfg) * world / (ms_per_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (prefill): HBM-bound at this window
+    achieved = prefill_bytes(cfg) / (prefill_ms * 1e-3) / 1e9
+    roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=args.traffic,
+                    kernel="swa_prefill_kernel<128>", us_per_launch=round(prefill_ms * 1e3, 2),
+                    peak_source=peaks["source"],
+                    tensor_tflops=round(4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] *
+                                        pairs_per_head(cfg["L"], cfg["w"], cfg["s"]) /
+                                        (prefill_ms * 1e-3) / 1e12, 2))
+
+    dec = bench_decode(swa, device, stream) if rank == 0 else None
+    e2e = run_e2e(swa, cfg, host_sets[0], device, stream, max(3, min(K, 20)), world)
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": "SWA(w,s) prefill in-band TFLOP/s & decode KV GB/s, % of B300 roofline",
+            "value": round(value, 3),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/k/v, sink keys x4)",
+            "config": {"workload": cfg["name"], "B": cfg["B"], "L": cfg["L"], "Hq": cfg["Hq"],
+                       "Hkv": cfg["Hkv"], "d": cfg["d"], "w": cfg["w"], "s": cfg["s"],
+                       "global_batch": cfg["B"] * world, "seq_len": cfg["L"],
+                       "parallelism": f"replicas x{world}",
+                       "step": "prefill + append(prompt) + append(1) + decode(pos=L)",
+                       "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
+                             f"(> 126 MB L2), CUDA graph per set"},
+            "roofline": roofline,
+            "decode": dict(workload=DECODE["name"], value=round(dec["gbs"], 1), unit="GB/s",
+                           bound="hbm", peak=peaks["hbm_gbs"],
+                           frac=round(dec["gbs"] / peaks["hbm_gbs"], 4),
+                           us_per_launch=round(dec["us_per_launch"], 3),
+                           kv_bytes_per_launch=dec["kv_bytes_per_launch"],
+                           l2=f"{dec['caches']} distinct caches, {dec['pool_bytes'] / 1e6:.0f} MB"),
+            "e2e": e2e,
+            "gpu_launches": launches_per_step(swa, cfg) * K,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(cfg, host_sets[0], budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
+
+
+def run_e2e(swa, cfg, host, device, stream, K, world):
+    """The same step through the public API with host buffers: every step copies
+    the inputs from pinned host memory and reads the outputs back."""
+    pinned = {k: t.pin_memory() for k, t in host.items()}
+    out_h = torch.empty(cfg["B"], cfg["L"], cfg["Hq"], cfg["d"], dtype=torch.bfloat16).pin_memory()
+    dec_h = torch.empty(cfg["B"], cfg["Hq"], cfg["d"], dtype=torch.bfloat16).pin_memory()
+    st = GpuStep(swa, cfg, host, device)
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_h.numel() * 2 + dec_h.numel() * 2
+
+    def one():
+        for k, t in pinned.items():
+            st.dev[k].copy_(t, non_blocking=True)
+        st.prefill()
+        st.rest()
+        out_h.copy_(st.out, non_blocking=True)
+        dec_h.copy_(st.dec, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a.record(stream)
+        for _ in range(K):
+            one()
+        b.record(stream)
+        b.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / K, world, device)
+    return {"value": round(step_flops(cfg) * world / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": K}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def cpu_baseline(cfg, host, budget_s: float = 15.0):
+    """The fp64 oracle as it stands, on this host's cores, over a bounded sample
+    of the workload's query rows (all heads); throughput in in-band TFLOP/s."""
+    import oracle
+    cores = os.cpu_count() or 1
+    L, w, s = cfg["L"], cfg["w"], cfg["s"]
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(L, size=min(L, 64), replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.prefill(host["q"], host["k"], host["v"], w, s, 1.0 / math.sqrt(cfg["d"]), rows=probe,
+                   nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(L, max(64, len(probe) * budget_s / dt)))
+    rows = np.sort(rng.choice(L, size=n, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.prefill(host["q"], host["k"], host["v"], w, s, 1.0 / math.sqrt(cfg["d"]), rows=rows,
+                   nthreads=cores)
+    dt = time.perf_counter() - t0
+    pairs = sum(keys_of_row(int(t), w, s) for t in rows)
+    flops = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * pairs
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{n} of {L} query rows x {cfg['Hq']} heads of the prefill "
+                      f"(fp64, OpenMP over rows)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    cfg = WORKLOAD
+    host = make_step_inputs(cfg, 1, None)[0]
+    import oracle
+    cores = os.cpu_count() or 1
+    L, w, s = cfg["L"], cfg["w"], cfg["s"]
+    rows_per_step = max(8, int(args.ref_rows))
+    rng = np.random.default_rng(1)
+    sc = 1.0 / math.sqrt(cfg["d"])
+    for _ in range(args.warmup):
+        r = np.sort(rng.choice(L, size=min(L, 8), replace=False)).astype(np.int64)
+        oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=r, nthreads=cores)
+    total_t, total_flops = 0.0, 0.0
+    for _ in range(args.steps):
+        r = np.sort(rng.choice(L, size=min(L, rows_per_step), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=r, nthreads=cores)
+        total_t += time.perf_counter() - t0
+        total_flops += 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * sum(keys_of_row(int(t), w, s)
+                                                                     for t in r)
+    value = total_flops / total_t / 1e12
+    sample = f"{rows_per_step} random query rows x {cfg['Hq']} heads per step (fp64 oracle)"
+    return {
+        "impl": "reference",
+        "metric": "SWA(w,s) prefill in-band TFLOP/s & decode KV GB/s, % of B300 roofline",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total_t / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/k/v, sink keys x4)",
+        "config": {"workload": cfg["name"], "B": cfg["B"], "L": cfg["L"], "Hq": cfg["Hq"],
+                   "Hkv": cfg["Hkv"], "d": cfg["d"], "w": cfg["w"], "s": cfg["s"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per prefill launch from an ncu capture of this kernel")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+/*
+ * swa.h -- C ABI of libswa.so: causal sliding-window attention with attention
+ * sinks, SWA(w, s), on NVIDIA B300 (sm_103a).
+ *
+ * The operation (explainer page of arXiv 2608.28444, "滑动窗口注意力（SWA）配
+ * sinks 比 post-training 线性注意力更划算", section "核心方法 / 1. 训练免费的
+ * SWA(w, s)": the x_t equation and the swa_mask definition):
+ *
+ *   query t (0-indexed) attends to the key set
+ *       K(t) = { j : j <= t  and  (j >= t - w + 1  or  j < s) },
+ *   i.e. the last w tokens (t itself included) plus the first s tokens
+ *   ("sinks"), and returns  sum_{j in K(t)} softmax_j(scale * q_t . k_j) v_j.
+ *
+ * Query head hq reads key/value head hq / (Hq / Hkv) (grouped-query attention;
+ * wiblog.cn long-context SWA article, section "SWA 的核心机制", Mistral 7B with
+ * 8 KV heads). Decode runs over a rolling KV cache of s pinned sink slots plus w
+ * window slots (same article, section "与 KV Cache 的配合：轮转替换策略").
+ *
+ * Conventions for every call:
+ *  - Tensors are dense, row-major, bf16 (2 bytes per element) unless stated;
+ *    the last dimension (d) is contiguous. All tensor pointers are DEVICE
+ *    pointers owned by the caller; the library keeps no pointer after a call
+ *    returns and allocates no device memory.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (NULL = legacy default stream) and
+ *    never synchronises. Argument errors are detected on the host before any
+ *    launch; nothing is launched in that case.
+ *  - Inputs must be finite. scale must be finite and > 0.
+ *  - Return value: SWA_OK, or an SWA_ERR_* code; swa_last_error() gives a
+ *    text description of the last failure on the calling thread.
+ *  - Supported head dimensions: d in {64, 128}. Group size Hq / Hkv in 1..128.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SWA_API __attribute__((visibility("default")))
+#else
+#define SWA_API
+#endif
+
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st *swa_stream_t;
+
+enum swa_status {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = 1, /* null pointer, bad size, w < 1, Hq % Hkv != 0 ... */
+    SWA_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d = 96)   */
+    SWA_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed         */
+    SWA_ERR_DEVICE = 4       /* no usable sm_103a device                       */
+};
+
+/* Prefill: out = SWA(w, s) attention of every query of a prompt.
+ *   q   [B, L, Hq,  d]  bf16        k, v [B, L, Hkv, d]  bf16
+ *   out [B, L, Hq,  d]  bf16 (written; must not alias q, k or v)
+ * Requires B, L >= 1, w >= 1, s >= 0, Hq % Hkv == 0. w >= L gives full causal
+ * attention; s > 0 adds the sinks. Accumulation is fp32, probabilities are
+ * rounded to bf16 before the value product, the output is rounded to bf16
+ * (round to nearest even). Only key tiles that intersect a query block's
+ * window, plus the sink tile, are loaded or multiplied (explainer of
+ * "Hybrid Sliding Window Attention", section "三、3. FlashAttention-2 /
+ * FlashAttention-3": tiles outside the window are skipped). */
+SWA_API int swa_prefill(const void *q, const void *k, const void *v, void *out,
+                int B, int L, int Hq, int Hkv, int d, int w, int s,
+                float scale, swa_stream_t stream);
+
+/* Ring-cache append: store T consecutive new tokens of every sequence.
+ *   k_new, v_new [B, T, Hkv, d] bf16     kcache, vcache [B, Hkv, s + w, d] bf16
+ *   pos_start    DEVICE int32[B]: position of token 0 of this call, per sequence
+ * Token i of sequence b has position p = pos_start[b] + i and goes to slot
+ *   slot(p) = p                   if p < s      (sink slots, kept forever)
+ *           = s + (p - s) mod w   otherwise     (window slots, oldest evicted)
+ * Tokens that a later token of the same call evicts again are not written.
+ * Positions must be appended in order across calls (each call continues where
+ * the previous one ended); positions < 0 are skipped and flagged in the
+ * device error word. */
+SWA_API int swa_cache_append(const void *k_new, const void *v_new, void *kcache, void *vcache,
+                     const int *pos_start, int B, int T, int Hkv, int d, int w, int s,
+                     swa_stream_t stream);
+
+/* Bytes of device workspace swa_decode needs for these sizes (0 if none). */
+SWA_API size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s);
+
+/* Decode: one new query per head attends over the ring cache.
+ *   q   [B, Hq, d] bf16; out [B, Hq, d] bf16 (written)
+ *   kcache, vcache [B, Hkv, s + w, d] bf16, already holding position pos[b]
+ *   pos DEVICE int32[B]: position of the newest token of each sequence.
+ * The cache then holds exactly K(pos) in its first min(pos + 1, s + w) slots,
+ * so no masking is needed. workspace: caller-owned device memory of at least
+ * swa_decode_workspace_size(...) bytes (may be NULL when that is 0). */
+SWA_API int swa_decode(const void *q, const void *kcache, const void *vcache, const int *pos,
+               void *out, int B, int Hq, int Hkv, int d, int w, int s, float scale,
+               void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
+/* Host helper: the cache slot of position pos (the formula above), or -1 for
+ * pos < 0, w < 1 or s < 0. */
+SWA_API long long swa_cache_slot(long long pos, int w, int s);
+
+/* Host helper: bytes of ONE cache tensor (K or V) [B, Hkv, s + w, d] bf16. */
+SWA_API size_t swa_cache_bytes(int B, int Hkv, int d, int w, int s);
+
+/* Host helper: the prefill tiling the library picks for these sizes.
+ * plan[0] query positions per block (Tq)      plan[1] tile rows (Tq * Hq/Hkv)
+ * plan[2] keys per band tile                  plan[3] keys per sink tile (0: none)
+ * plan[4] sink tiles per block                plan[5] K/V pipeline stages
+ * plan[6] persistent CTAs on the current device (0 without a device)
+ * plan[7] dynamic shared memory bytes per CTA */
+SWA_API int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]);
+
+/* Test aid: the (query, key) pairs that the prefill kernel's tile schedule and
+ * in-tile masks admit, for rows row0 .. row0 + nrows - 1 of a prompt of length
+ * L, with the same tiling as swa_prefill for these sizes.
+ *   bits   DEVICE uint32 [nrows, ceil(L / 32)]: bit (j % 32) of word j / 32 of
+ *          row r is set iff key j is admitted for query row0 + r
+ *   counts DEVICE int32 [nrows]: admitted pairs counted over all tiles (equals
+ *          the popcount of the row only if no key is admitted twice) */
+SWA_API int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
+                      uint32_t *bits, int *counts, swa_stream_t stream);
+
+/* Test aid: the same admitted-pair bitmask and counts as swa_debug_keymask,
+ * computed on the host by the library's host copy of the schedule (no device
+ * needed). bits and counts are HOST arrays of the same shapes. */
+SWA_API int swa_keymask_host(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
+                     uint32_t *bits, int *counts);
+
+/* Read the device error word that kernels set instead of trapping (a bounded
+ * wait that gave up, a negative position). *code receives 0 if no error was
+ * recorded. Synchronises the current device. clear != 0 resets it to 0. */
+SWA_API int swa_device_error(int *code, int clear);
+
+SWA_API const char *swa_status_string(int status);
+SWA_API const char *swa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,282 @@
+"""Python binding of libswa.so: SWA(w, s) prefill, ring-cache append and decode
+on NVIDIA B300 (sm_103a).
+
+The functions below only marshal arguments (shape checks, pointers, the
+current CUDA stream) and call the C ABI declared in ``include/swa.h``; every
+step of the computation runs in the library's CUDA kernels. There is no CPU
+or PyTorch fallback: if ``libswa.so`` is missing, importing this package
+raises ImportError (build it with ``python sliding_window_attention_05_b300/build.py``).
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "swa.h")
+
+SWA_OK = 0
+SWA_ERR_INVALID_ARG = 1
+SWA_ERR_UNSUPPORTED = 2
+SWA_ERR_CUDA = 3
+SWA_ERR_DEVICE = 4
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python sliding_window_attention_05_b300/build.py`"
+        " (the SWA kernels have no fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_lib.swa_prefill.restype = _i
+_lib.swa_prefill.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.swa_cache_append.restype = _i
+_lib.swa_cache_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
+_lib.swa_decode_workspace_size.restype = _sz
+_lib.swa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+_lib.swa_decode.restype = _i
+_lib.swa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+_lib.swa_cache_slot.restype = ctypes.c_longlong
+_lib.swa_cache_slot.argtypes = [ctypes.c_longlong, _i, _i]
+_lib.swa_cache_bytes.restype = _sz
+_lib.swa_cache_bytes.argtypes = [_i, _i, _i, _i, _i]
+_lib.swa_prefill_plan.restype = _i
+_lib.swa_prefill_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]
+_lib.swa_debug_keymask.restype = _i
+_lib.swa_debug_keymask.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+_lib.swa_keymask_host.restype = _i
+_lib.swa_keymask_host.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp]
+_lib.swa_device_error.restype = _i
+_lib.swa_device_error.argtypes = [ctypes.POINTER(_i), _i]
+_lib.swa_status_string.restype = ctypes.c_char_p
+_lib.swa_status_string.argtypes = [_i]
+_lib.swa_last_error.restype = ctypes.c_char_p
+_lib.swa_last_error.argtypes = []
+
+
+class SwaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.swa_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {_lib.swa_status_string(status).decode()} ({msg})")
+
+
+def _check(status: int, where: str):
+    if status != SWA_OK:
+        raise SwaError(status, where)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libswa.so (for calling the C ABI directly)."""
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/swa.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _bf16_cuda(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _default_scale(d: int, scale):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+# ---------------------------------------------------------------- prefill
+
+def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
+                scale: float | None = None, out: torch.Tensor | None = None, stream=None):
+    """SWA(w, s) prefill. q [B,L,Hq,d], k/v [B,L,Hkv,d] bf16 -> out [B,L,Hq,d].
+
+    CUDA tensors run asynchronously on the current stream. CPU tensors are the
+    host-buffer path: they are copied to the current device, the kernel runs,
+    and the result is copied back to a (pinned) host tensor before returning.
+    """
+    if not q.is_cuda:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
+        od = swa_prefill(qd, kd, vd, w, s, scale, None, stream)
+        host = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        host.copy_(od, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return host
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _bf16_cuda(t, n)
+    B, L, Hq, d = q.shape
+    if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _bf16_cuda(out, "out")
+    _check(_lib.swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, L, Hq, Hkv, d, int(w),
+                            int(s), _default_scale(d, scale), _stream(stream)), "swa_prefill")
+    return out
+
+
+prefill = swa_prefill
+
+
+def swa_prefill_plan(L: int, Hq: int, Hkv: int, d: int, w: int, s: int) -> dict:
+    plan = (_i * 8)()
+    _check(_lib.swa_prefill_plan(L, Hq, Hkv, d, w, s, plan), "swa_prefill_plan")
+    keys = ("Tq", "rows", "n_band", "s_box", "n_sink", "stages", "ctas", "smem_bytes")
+    return dict(zip(keys, list(plan)))
+
+
+# ---------------------------------------------------------------- ring cache
+
+def swa_cache_slot(pos: int, w: int, s: int) -> int:
+    return int(_lib.swa_cache_slot(int(pos), int(w), int(s)))
+
+
+def swa_cache_bytes(B: int, Hkv: int, d: int, w: int, s: int) -> int:
+    return int(_lib.swa_cache_bytes(B, Hkv, d, w, s))
+
+
+def swa_cache_append(k_new: torch.Tensor, v_new: torch.Tensor, kcache: torch.Tensor,
+                     vcache: torch.Tensor, pos_start: torch.Tensor, w: int, s: int, stream=None):
+    """Append tokens k_new/v_new [B,T,Hkv,d] at positions pos_start[b] + i."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"), (vcache, "vcache")):
+        _bf16_cuda(t, n)
+    if pos_start.dtype != torch.int32 or not pos_start.is_cuda:
+        raise TypeError("pos_start must be a CUDA int32 tensor")
+    B, T, Hkv, d = k_new.shape
+    if kcache.shape != (B, Hkv, s + w, d) or vcache.shape != kcache.shape:
+        raise ValueError(f"cache must be [B, Hkv, s + w, d] = {(B, Hkv, s + w, d)}")
+    _check(_lib.swa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                                 _ptr(pos_start), B, T, Hkv, d, int(w), int(s), _stream(stream)),
+           "swa_cache_append")
+
+
+def swa_decode_workspace_size(B: int, Hq: int, Hkv: int, d: int, w: int, s: int) -> int:
+    return int(_lib.swa_decode_workspace_size(B, Hq, Hkv, d, w, s))
+
+
+def swa_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, pos: torch.Tensor,
+               w: int, s: int, scale: float | None = None, out: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None, stream=None):
+    """One decode step: q [B,Hq,d] over the ring cache holding position pos[b]."""
+    for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
+        _bf16_cuda(t, n)
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError("pos must be a CUDA int32 tensor")
+    B, Hq, d = q.shape
+    Hkv = kcache.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    need = swa_decode_workspace_size(B, Hq, Hkv, d, w, s)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.swa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(pos), _ptr(out), B, Hq, Hkv,
+                           d, int(w), int(s), _default_scale(d, scale), _ptr(workspace), wbytes,
+                           _stream(stream)), "swa_decode")
+    return out
+
+
+cache_append = swa_cache_append
+decode = swa_decode
+
+
+class RingCache:
+    """A rolling KV cache of s sink slots + w window slots per (sequence, KV
+    head), in device memory owned by this object (allocated through PyTorch)."""
+
+    def __init__(self, B: int, Hkv: int, d: int, w: int, s: int, device=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self.B, self.Hkv, self.d, self.w, self.s = B, Hkv, d, w, s
+        self.k = torch.zeros(B, Hkv, s + w, d, dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.next_pos = torch.zeros(B, dtype=torch.int32, device=device)
+        self._last_pos = torch.zeros(B, dtype=torch.int32, device=device)
+        self._workspace = None
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """Append [B, T, Hkv, d] tokens after the ones already held."""
+        T = k_new.shape[1]
+        swa_cache_append(k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s, stream)
+        self._last_pos.copy_(self.next_pos + (T - 1))
+        self.next_pos.add_(T)
+
+    def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):
+        """Attend q [B, Hq, d] (the newest token's queries) over the cache."""
+        B, Hq, d = q.shape
+        need = swa_decode_workspace_size(B, Hq, self.Hkv, d, self.w, self.s)
+        if need and (self._workspace is None or self._workspace.numel() < need):
+            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        return swa_decode(q, self.k, self.v, self._last_pos, self.w, self.s, scale, out,
+                          self._workspace if need else None, stream)
+
+
+# ---------------------------------------------------------------- test aids
+
+def swa_debug_keymask(L: int, Hq: int, Hkv: int, d: int, w: int, s: int, row0: int, nrows: int,
+                      device=None):
+    """Admitted (row, key) pairs of the prefill schedule, computed on the GPU:
+    returns (bits uint32 [nrows, ceil(L/32)], counts int32 [nrows]) on the device."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    words = (L + 31) // 32
+    bits = torch.empty(nrows, words, dtype=torch.int32, device=device)
+    counts = torch.empty(nrows, dtype=torch.int32, device=device)
+    _check(_lib.swa_debug_keymask(L, Hq, Hkv, d, w, s, row0, nrows, _ptr(bits), _ptr(counts),
+                                  _stream(None)), "swa_debug_keymask")
+    return bits, counts
+
+
+def swa_keymask_host(L: int, Hq: int, Hkv: int, d: int, w: int, s: int, row0: int, nrows: int):
+    """The same admitted-pair bitmask, computed by the library's host copy of
+    the schedule (no GPU needed)."""
+    words = (L + 31) // 32
+    bits = torch.zeros(nrows, words, dtype=torch.int32)
+    counts = torch.zeros(nrows, dtype=torch.int32)
+    _check(_lib.swa_keymask_host(L, Hq, Hkv, d, w, s, row0, nrows, _ptr(bits), _ptr(counts)),
+           "swa_keymask_host")
+    return bits, counts
+
+
+def swa_device_error(clear: bool = True) -> int:
+    code = _i(0)
+    _check(_lib.swa_device_error(ctypes.byref(code), 1 if clear else 0), "swa_device_error")
+    return code.value
+
+
+def swa_status_string(status: int) -> str:
+    return _lib.swa_status_string(status).decode()
+
+
+def swa_last_error() -> str:
+    return _lib.swa_last_error().decode(errors="replace")

@@ -1,0 +1,455 @@
+// swa_api.cu -- the C ABI of libswa.so (declared in include/swa.h).
+//
+// One translation unit holds every kernel so the device error word needs no
+// relocatable device code. The library allocates no device memory: all
+// tensors and the decode workspace are the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/swa.h"
+#include "decode.cuh"
+#include "prefill.cuh"
+#include "sm100_ptx.cuh"
+#include "swa_index.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(SWA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_d(int d) { return d == 64 || d == 128; }
+
+// ------------------------------------------------------------------ device info
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem_optin = 0;
+  bool ok = false;
+};
+
+int current_device_info(DeviceInfo *info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return fail(SWA_ERR_DEVICE, "device ordinal %d out of range", dev);
+  if (!cache[dev].ok) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(SWA_ERR_DEVICE, "libswa.so is built for sm_103a; device %d is sm_%d%d", dev,
+                  major, minor);
+    cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&cache[dev].max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                           dev);
+    cache[dev].ok = true;
+  }
+  *info = cache[dev];
+  return SWA_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 map over a [B, L, H, d] tensor (dims listed innermost first) with
+// a box of 64 x box_h x box_l x 1 and the 128-byte swizzle.
+int make_map_bf16_4d(CUtensorMap *map, const void *base, int B, int L, int H, int d, int box_h,
+                     int box_l) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)L * H * d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_h, (cuuint32_t)box_l, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SWA_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+
+int prefill_stages(int d, int max_smem) {
+  const long long qb = (long long)(d / 64) * swa::kChunkBytes;
+  const long long fixed = 1024 + 256 + 2 * qb + swa::kPBytes;
+  long long st = (max_smem - fixed) / qb;
+  if (st > 8) st = 8;
+  return (int)st;
+}
+
+template <int D>
+int launch_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
+                   int Hkv, int w, int s, float scale, cudaStream_t stream,
+                   const DeviceInfo &dev) {
+  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  CUtensorMap tq, tk, tv, tks, tvs;
+  int rc;
+  if ((rc = make_map_bf16_4d(&tq, q, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+  if ((rc = make_map_bf16_4d(&tk, k, B, L, Hkv, D, 1, plan.n_band))) return rc;
+  if ((rc = make_map_bf16_4d(&tv, v, B, L, Hkv, D, 1, plan.n_band))) return rc;
+  if (plan.n_sink > 0) {
+    if ((rc = make_map_bf16_4d(&tks, k, B, L, Hkv, D, 1, plan.s_box))) return rc;
+    if ((rc = make_map_bf16_4d(&tvs, v, B, L, Hkv, D, 1, plan.s_box))) return rc;
+  } else {
+    tks = tk;
+    tvs = tv;
+  }
+  const int stages = prefill_stages(D, dev.max_smem_optin);
+  if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
+  const size_t smem = swa::PrefillSmem<D>::bytes(stages);
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(swa::swa_prefill_kernel<D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    dev.max_smem_optin);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
+
+  swa::PrefillArgs a;
+  a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  a.B = B;
+  a.L = L;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.w = w;
+  a.s = s;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.plan = plan;
+  a.n_items = B * Hkv * plan.nqb;
+  a.stages = stages;
+  const int grid = swa::imin(a.n_items, dev.sms);
+  swa::swa_prefill_kernel<D><<<grid, swa::kPrefillThreads, smem, stream>>>(tq, tk, tv, tks, tvs, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill launch");
+  return SWA_OK;
+}
+
+// ------------------------------------------------------------------ decode
+
+constexpr int kDecodeTargetCtas = 296;  // two waves' worth of CTAs on 148 SMs
+constexpr int kDecodeMinKeysPerSplit = 64;
+
+int head_group(int G) {
+  if (G % 8 == 0) return 8;
+  if (G % 4 == 0) return 4;
+  if (G % 2 == 0) return 2;
+  return 1;
+}
+
+int decode_splits(int B, int Hq, int Hkv, int w, int s) {
+  const int G = Hq / Hkv;
+  const long long units = (long long)B * Hkv * (G / head_group(G));
+  if (units >= kDecodeTargetCtas) return 1;
+  long long sp = (kDecodeTargetCtas + units - 1) / units;
+  const long long cap = ((long long)s + w + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
+  if (sp > cap) sp = cap;
+  if (sp < 1) sp = 1;
+  return (int)sp;
+}
+
+size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
+  const int sp = decode_splits(B, Hq, Hkv, w, s);
+  if (sp <= 1) return 0;
+  const size_t n = (size_t)B * Hq * sp;
+  return n * d * sizeof(float) + n * sizeof(float2);
+}
+
+template <int D, int HG>
+cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
+  const int G = a.Hq / a.Hkv;
+  dim3 grid(a.splits, a.Hkv * (G / HG), B);
+  swa::swa_decode_kernel<D, HG><<<grid, swa::kDecodeWarps * 32, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  swa::swa_decode_combine_kernel<D><<<B * a.Hq, D, 0, stream>>>(a.part_o, a.part_ml, a.out,
+                                                               a.splits);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
+  switch (head_group(a.Hq / a.Hkv)) {
+    case 8: return launch_decode_t<D, 8>(a, B, stream);
+    case 4: return launch_decode_t<D, 4>(a, B, stream);
+    case 2: return launch_decode_t<D, 2>(a, B, stream);
+    default: return launch_decode_t<D, 1>(a, B, stream);
+  }
+}
+
+int check_heads(int Hq, int Hkv) {
+  if (Hq < 1 || Hkv < 1) return fail(SWA_ERR_INVALID_ARG, "Hq and Hkv must be >= 1");
+  if (Hq % Hkv != 0) return fail(SWA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Hq / Hkv > 128) return fail(SWA_ERR_UNSUPPORTED, "group size Hq/Hkv > 128");
+  return SWA_OK;
+}
+
+int check_scale(float scale) {
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(SWA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  return SWA_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char *swa_status_string(int status) {
+  switch (status) {
+    case SWA_OK: return "ok";
+    case SWA_ERR_INVALID_ARG: return "invalid argument";
+    case SWA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SWA_ERR_CUDA: return "CUDA error";
+    case SWA_ERR_DEVICE: return "no usable sm_103a device";
+    default: return "unknown status";
+  }
+}
+
+const char *swa_last_error(void) { return g_last_error; }
+
+long long swa_cache_slot(long long pos, int w, int s) {
+  if (pos < 0 || w < 1 || s < 0) return -1;
+  return swa::ring_slot(pos, w, s);
+}
+
+size_t swa_cache_bytes(int B, int Hkv, int d, int w, int s) {
+  if (B < 0 || Hkv < 0 || d < 0 || w < 0 || s < 0) return 0;
+  return (size_t)B * Hkv * ((size_t)s + w) * d * 2;
+}
+
+int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]) {
+  if (!plan) return fail(SWA_ERR_INVALID_ARG, "plan is NULL");
+  if (L < 1 || w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need L >= 1, w >= 1, s >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  const swa::PrefillPlan p = swa::make_plan(L, Hq, Hkv, w, s);
+  plan[0] = p.Tq;
+  plan[1] = p.rows;
+  plan[2] = p.n_band;
+  plan[3] = p.s_box;
+  plan[4] = p.n_sink;
+  plan[5] = prefill_stages(d, 232448);
+  plan[6] = 0;
+  plan[7] = 0;
+  int dev_count = 0;
+  if (cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0) {
+    DeviceInfo dev;
+    if (current_device_info(&dev) == SWA_OK) {
+      plan[5] = prefill_stages(d, dev.max_smem_optin);
+      plan[6] = dev.sms;
+      plan[7] = (int)(d == 64 ? swa::PrefillSmem<64>::bytes(plan[5]) : swa::PrefillSmem<128>::bytes(plan[5]));
+    }
+  } else {
+    cudaGetLastError();
+  }
+  return SWA_OK;
+}
+
+int swa_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
+                int Hkv, int d, int w, int s, float scale, swa_stream_t stream) {
+  if (!q || !k || !v || !out) return fail(SWA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || L < 1) return fail(SWA_ERR_INVALID_ARG, "B and L must be >= 1");
+  if (w < 1) return fail(SWA_ERR_INVALID_ARG, "window w must be >= 1");
+  if (s < 0) return fail(SWA_ERR_INVALID_ARG, "sink count s must be >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if ((rc = check_scale(scale))) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if ((long long)B * Hkv * swa::cdiv(L, 128 / (Hq / Hkv)) > 0x7FFFFFFFll)
+    return fail(SWA_ERR_UNSUPPORTED, "too many query blocks");
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64) return launch_prefill<64>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev);
+  return launch_prefill<128>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev);
+}
+
+int swa_cache_append(const void *k_new, const void *v_new, void *kcache, void *vcache,
+                     const int *pos_start, int B, int T, int Hkv, int d, int w, int s,
+                     swa_stream_t stream) {
+  if (!k_new || !v_new || !kcache || !vcache || !pos_start)
+    return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kcache) || !aligned16(vcache))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || T < 1 || Hkv < 1) return fail(SWA_ERR_INVALID_ARG, "B, T and Hkv must be >= 1");
+  if (w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need w >= 1 and s >= 0");
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if (B > 65535) return fail(SWA_ERR_UNSUPPORTED, "B > 65535");
+  DeviceInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc) return rc;
+  const long long n = (long long)T * Hkv * (d / 8);
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "append too large");
+  swa::swa_append_kernel<<<dim3((unsigned)blocks, B), threads, 0,
+                           reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
+      reinterpret_cast<uint4 *>(kcache), reinterpret_cast<uint4 *>(vcache), pos_start, T, Hkv, d,
+      w, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "swa_cache_append launch");
+  return SWA_OK;
+}
+
+size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || !supported_d(d)) return 0;
+  return decode_workspace(B, Hq, Hkv, d, w, s);
+}
+
+int swa_decode(const void *q, const void *kcache, const void *vcache, const int *pos, void *out,
+               int B, int Hq, int Hkv, int d, int w, int s, float scale, void *workspace,
+               size_t workspace_bytes, swa_stream_t stream) {
+  if (!q || !kcache || !vcache || !pos || !out) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1) return fail(SWA_ERR_INVALID_ARG, "B must be >= 1");
+  if (w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need w >= 1 and s >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if ((rc = check_scale(scale))) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if (B > 65535 || Hq > 65535) return fail(SWA_ERR_UNSUPPORTED, "B or Hq > 65535");
+  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return fail(SWA_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required, got %zu",
+                need, workspace ? workspace_bytes : (size_t)0);
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  swa::DecodeArgs a;
+  a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+  a.kc = reinterpret_cast<const __nv_bfloat16 *>(kcache);
+  a.vc = reinterpret_cast<const __nv_bfloat16 *>(vcache);
+  a.pos = pos;
+  a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.w = w;
+  a.s = s;
+  a.splits = decode_splits(B, Hq, Hkv, w, s);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const size_t n = (size_t)B * Hq * a.splits;
+  a.part_o = a.splits > 1 ? reinterpret_cast<float *>(workspace) : nullptr;
+  a.part_ml = a.splits > 1 ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(workspace) +
+                                                        n * d * sizeof(float))
+                           : nullptr;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = d == 64 ? launch_decode_d<64>(a, B, st) : launch_decode_d<128>(a, B, st);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_decode launch");
+  return SWA_OK;
+}
+
+int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
+                      uint32_t *bits, int *counts, swa_stream_t stream) {
+  if (!bits || !counts) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (L < 1 || w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need L >= 1, w >= 1, s >= 0");
+  if (row0 < 0 || nrows < 1 || (long long)row0 + nrows > L)
+    return fail(SWA_ERR_INVALID_ARG, "rows [%d, %d) outside [0, %d)", row0, row0 + nrows, L);
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  swa::swa_keymask_kernel<<<nrows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      plan, L, w, s, row0, nrows, bits, counts);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "swa_debug_keymask launch");
+  return SWA_OK;
+}
+
+int swa_keymask_host(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
+                     uint32_t *bits, int *counts) {
+  if (!bits || !counts) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (L < 1 || w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need L >= 1, w >= 1, s >= 0");
+  if (row0 < 0 || nrows < 1 || (long long)row0 + nrows > L)
+    return fail(SWA_ERR_INVALID_ARG, "rows [%d, %d) outside [0, %d)", row0, row0 + nrows, L);
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  const int words = swa::cdiv(L, 32);
+  for (int r = 0; r < nrows; ++r) {
+    const int t = row0 + r;
+    uint32_t *row_bits = bits + (size_t)r * words;
+    for (int i = 0; i < words; ++i) row_bits[i] = 0u;
+    int cnt = 0;
+    const swa::BlockTiles bt = swa::block_tiles(plan, t / plan.Tq, L, w, s);
+    for (int i = 0; i < bt.n_tiles; ++i) {
+      const swa::Tile tl = swa::tile_at(plan, bt, i, w, s);
+      for (int c = 0; c < tl.ncols; ++c) {
+        const int j = tl.k0 + c;
+        if ((tl.full || swa::admit(t, j, w, s, tl.own_lo, tl.own_hi)) && j >= 0 && j < L) {
+          row_bits[j / 32] |= 1u << (j % 32);
+          ++cnt;
+        }
+      }
+    }
+    counts[r] = cnt;
+  }
+  return SWA_OK;
+}
+
+int swa_device_error(int *code, int clear) {
+  if (!code) return fail(SWA_ERR_INVALID_ARG, "code is NULL");
+  DeviceInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpyFromSymbol(code, swa::g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (clear) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(swa::g_device_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  }
+  return SWA_OK;
+}
+
+}  // extern "C"
