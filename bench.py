@@ -330,8 +330,9 @@ def run_gpu(args):
                                         pairs_per_head(cfg["L"], cfg["w"], cfg["s"]) /
                                         (prefill_ms * 1e-3) / 1e12, 2))
 
-    dec = bench_decode(swa, device, stream) if rank == 0 else None
-    e2e = run_e2e(swa, cfg, host_sets[0], device, stream, max(3, min(K, 20)), world)
+    dec = bench_decode(swa, device, stream) if (rank == 0 and not args.skip_decode) else None
+    e2e = None if args.skip_e2e else run_e2e(swa, cfg, host_sets[0], device, stream,
+                                               max(3, min(K, 20)), world)
 
     result = None
     if rank == 0:
@@ -356,12 +357,12 @@ def run_gpu(args):
                        "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
                              f"(> 126 MB L2), CUDA graph per set"},
             "roofline": roofline,
-            "decode": dict(workload=DECODE["name"], value=round(dec["gbs"], 1), unit="GB/s",
-                           bound="hbm", peak=peaks["hbm_gbs"],
-                           frac=round(dec["gbs"] / peaks["hbm_gbs"], 4),
-                           us_per_launch=round(dec["us_per_launch"], 3),
-                           kv_bytes_per_launch=dec["kv_bytes_per_launch"],
-                           l2=f"{dec['caches']} distinct caches, {dec['pool_bytes'] / 1e6:.0f} MB"),
+            "decode": None if dec is None else dict(
+                workload=DECODE["name"], value=round(dec["gbs"], 1), unit="GB/s",
+                bound="hbm", peak=peaks["hbm_gbs"], frac=round(dec["gbs"] / peaks["hbm_gbs"], 4),
+                us_per_launch=round(dec["us_per_launch"], 3),
+                kv_bytes_per_launch=dec["kv_bytes_per_launch"],
+                l2=f"{dec['caches']} distinct caches, {dec['pool_bytes'] / 1e6:.0f} MB"),
             "e2e": e2e,
             "gpu_launches": launches_per_step(swa, cfg) * K,
             "clocks": clk.summary(),
@@ -490,6 +491,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

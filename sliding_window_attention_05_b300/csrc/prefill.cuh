@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_init(&q_empty[1], 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
     mbar_init(o_full, 1);
     mbar_init(mma_done, 1);
@@ -292,30 +292,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc_fence_after();
         float x[128];
         const uint32_t s_addr = lane_addr + kTmemS0 + (g & 1) * 128;
+        const int nch = tl.ncols >> 4;  // 16-column chunks (ncols is a multiple of 16)
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          if (c * 16 < tl.ncols) tmem_ld16(s_addr + c * 16, *reinterpret_cast<float(*)[16]>(&x[c * 16]));
+          if (c < nch) tmem_ld16(s_addr + c * 16, *reinterpret_cast<float(*)[16]>(&x[c * 16]));
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          if (c * 16 < tl.ncols) reg_fence16(*reinterpret_cast<float(*)[16]>(&x[c * 16]));
-        float m_tile = -INFINITY;
-        if (tl.full) {
+          if (c < nch) reg_fence16(*reinterpret_cast<float(*)[16]>(&x[c * 16]));
+        if (!tl.full) {
+          // The admitted columns of this row form at most two ranges: the
+          // window part [max(own_lo, t-w+1), min(own_hi, t+1)) and the sink
+          // part [own_lo, min(own_hi, s, t+1)).
+          const int a_lo = imax(tl.own_lo, t - a.w + 1) - tl.k0;
+          const int a_hi = imin(tl.own_hi, t + 1) - tl.k0;
+          const int b_lo = tl.own_lo - tl.k0;
+          const int b_hi = imin(imin(tl.own_hi, a.s), t + 1) - tl.k0;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < tl.ncols) {
-              x[c] *= cl2;
-              m_tile = fmaxf(m_tile, x[c]);
-            }
-        } else {
+          for (int c = 0; c < 8; ++c)
+            if (c < nch) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < tl.ncols) {
-              const bool ok_c = admit(t, tl.k0 + c, a.w, a.s, tl.own_lo, tl.own_hi);
-              x[c] = ok_c ? x[c] * cl2 : -INFINITY;
-              m_tile = fmaxf(m_tile, x[c]);
+              for (int e = 0; e < 16; ++e) {
+                const int col = c * 16 + e;
+                const bool in = (col >= a_lo && col < a_hi) || (col >= b_lo && col < b_hi);
+                x[col] = in ? x[col] : -INFINITY;
+              }
             }
         }
+        // row max of the raw scores, eight independent chains
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[c * 16 + e]);
+          }
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mx8[0] = fmaxf(mx8[0], mx8[k]);
+        const float m_tile = mx8[0] * cl2;  // scale > 0, so the max commutes with it
         const float m_new = fmaxf(m_used, m_tile);
         float factor = 1.f;
         bool rescale = false;
@@ -328,25 +344,36 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           rescale = true;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float rs = 0.f;
+        float sum8[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < tl.ncols) {
-            x[c] = fast_exp2(x[c] - msub);
-            rs += x[c];
+        for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              x[c * 16 + e] = fast_exp2(fmaf(x[c * 16 + e], cl2, -msub));
+              sum8[e & 7] += x[c * 16 + e];
+            }
           }
+        float rs = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                   ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_sum += rs;
         // P buffer is free once the previous tile's P V has completed; that
         // also makes O current for the rescale below.
         if (g > 0 && !warp_wait(pv_done, (g - 1) & 1)) { ok = false; break; }
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (u * 8 < tl.ncols) {
-            const uint32_t addr = p_row + (u >> 3) * kChunkBytes + (((u & 7) ^ (r & 7)) << 4);
-            st_shared_v4(addr, pack_bf16x2(x[u * 8 + 0], x[u * 8 + 1]),
-                         pack_bf16x2(x[u * 8 + 2], x[u * 8 + 3]),
-                         pack_bf16x2(x[u * 8 + 4], x[u * 8 + 5]),
-                         pack_bf16x2(x[u * 8 + 6], x[u * 8 + 7]));
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int u = 2 * c + h;  // 16-byte unit: keys 8u .. 8u+7
+              const uint32_t addr = p_row + (u >> 3) * kChunkBytes + (((u & 7) ^ (r & 7)) << 4);
+              st_shared_v4(addr, pack_bf16x2(x[u * 8 + 0], x[u * 8 + 1]),
+                           pack_bf16x2(x[u * 8 + 2], x[u * 8 + 3]),
+                           pack_bf16x2(x[u * 8 + 4], x[u * 8 + 5]),
+                           pack_bf16x2(x[u * 8 + 6], x[u * 8 + 7]));
+            }
           }
         fence_proxy_async_smem();
         if (__any_sync(0xffffffffu, rescale)) {
@@ -363,7 +390,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);  // one arrival per softmax warp
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
