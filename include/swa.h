@@ -99,6 +99,36 @@ SWA_API int swa_decode(const void *q, const void *kcache, const void *vcache, co
                void *out, int B, int Hq, int Hkv, int d, int w, int s, float scale,
                void *workspace, size_t workspace_bytes, swa_stream_t stream);
 
+/* Maximum scratch bytes swa_decode_noalloc can use (see below). */
+#define SWA_DECODE_NOALLOC_SCRATCH_BYTES (2u << 20)
+
+/* Decode without any device allocation and without a caller workspace.
+ *
+ * (The pages have no counterpart: this is an interface convenience.)
+ *
+ * Same arguments, result and errors as swa_decode, minus the workspace. It is
+ * for callers that cannot allocate device memory at the point of the call --
+ * for example a serving loop whose engine owns all device memory in a fixed
+ * pool and forbids allocation during a step (cudaMalloc can synchronise the
+ * device and can fail under memory pressure), or plain C code that has no
+ * allocator of its own for scratch buffers. When swa_decode would need a
+ * split-KV workspace, this entry point uses a scratch array compiled into the
+ * library instead: SWA_DECODE_NOALLOC_SCRATCH_BYTES (2 MiB) of device memory
+ * that every GPU which loads libswa.so holds until the process exits.
+ *  - Sizes whose workspace (swa_decode_workspace_size) exceeds that maximum
+ *    are rejected with SWA_ERR_UNSUPPORTED before anything is launched.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on each device performs a one-time set-up (it looks up
+ *    the scratch array's device address with that device current). Make that
+ *    first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents;
+ *    nothing in it needs to start at zero. Calls whose kernels overlap on the
+ *    GPU (for example on two streams at once) race on it: order them on one
+ *    stream, or use swa_decode with a workspace each. */
+SWA_API int swa_decode_noalloc(const void *q, const void *kcache, const void *vcache,
+                               const int *pos, void *out, int B, int Hq, int Hkv, int d, int w,
+                               int s, float scale, swa_stream_t stream);
+
 /* Host helper: the cache slot of position pos (the formula above), or -1 for
  * pos < 0, w < 1 or s < 0. */
 SWA_API long long swa_cache_slot(long long pos, int w, int s);

@@ -48,6 +48,8 @@ _lib.swa_decode_workspace_size.restype = _sz
 _lib.swa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
 _lib.swa_decode.restype = _i
 _lib.swa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+_lib.swa_decode_noalloc.restype = _i
+_lib.swa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.swa_cache_slot.restype = ctypes.c_longlong
 _lib.swa_cache_slot.argtypes = [ctypes.c_longlong, _i, _i]
 _lib.swa_cache_bytes.restype = _sz

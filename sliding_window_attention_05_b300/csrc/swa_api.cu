@@ -232,6 +232,31 @@ int check_scale(float scale) {
   return SWA_OK;
 }
 
+// Scratch of swa_decode_noalloc: the split-KV partial results live here
+// instead of in a caller workspace. Every device that loads the library holds
+// it until exit; calls that overlap on the GPU share (and race on) it.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[SWA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (cudaGetSymbolAddress needs that device current).
+int noalloc_scratch_ptr(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SWA_ERR_DEVICE, "device ordinal %d out of range", dev);
+  static std::mutex mu;
+  static void *ptrs[64] = {nullptr};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return SWA_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -384,6 +409,27 @@ int swa_decode(const void *q, const void *kcache, const void *vcache, const int 
   cudaError_t e = d == 64 ? launch_decode_d<64>(a, B, st) : launch_decode_d<128>(a, B, st);
   if (e != cudaSuccess) return cuda_fail(e, "swa_decode launch");
   return SWA_OK;
+}
+
+int swa_decode_noalloc(const void *q, const void *kcache, const void *vcache, const int *pos,
+                       void *out, int B, int Hq, int Hkv, int d, int w, int s, float scale,
+                       swa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || !supported_d(d))
+    return swa_decode(q, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale, nullptr, 0,
+                      stream);  // let swa_decode report the argument error
+  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s);
+  if (need > SWA_DECODE_NOALLOC_SCRATCH_BYTES)
+    return fail(SWA_ERR_UNSUPPORTED,
+                "swa_decode_noalloc: these sizes need %zu bytes of scratch, above its fixed "
+                "maximum of %u bytes; use swa_decode with a workspace",
+                need, (unsigned)SWA_DECODE_NOALLOC_SCRATCH_BYTES);
+  void *scratch = nullptr;
+  if (need > 0) {
+    int rc = noalloc_scratch_ptr(&scratch);
+    if (rc) return rc;
+  }
+  return swa_decode(q, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale, scratch,
+                    need > 0 ? (size_t)SWA_DECODE_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 
 int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
