@@ -14,19 +14,23 @@
 //
 // Warp roles (256 threads, one CTA per SM):
 //   warp 0      TMA producer: Q (double buffered) and a ring of K/V tiles
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S_g = Q K_g^T  -> TMEM buffer g % 2   (tcgen05, fp32)
-//                 O  += P_g V_g  -> TMEM                 (tcgen05, fp32)
-//               S_{g+1} is issued before O += P_g V_g so the tensor core
-//               works on the next tile while the softmax warps finish this one
+//   warp 1      TMEM owner and MMA issuer (one thread), in the order
+//                 S_g = Q K_g^T      -> TMEM buffer g % 2      (fp32)
+//                 O  += P_{g-1} V_{g-1}                        (fp32)
+//               P_{g-1} is read from TMEM (it overwrites S_{g-1} in place), so
+//               the tensor core computes S_g while the softmax warps still
+//               work on tile g-1, and the softmax never waits for a P buffer.
 //   warps 4-7   softmax + epilogue, one thread per tile row (TMEM lane):
-//               in-tile mask, online softmax with lazy rescaling, P (bf16) to
-//               shared memory, O rescale in TMEM when the running max grows by
-//               more than 2^8, and at block end O / l -> bf16 -> global.
+//               in-tile mask (edge chunks only), online softmax with lazy
+//               rescaling, P (bf16) to TMEM, O rescale in TMEM when the running
+//               max grows by more than 2^8, and at block end O / l -> bf16.
 //
-// Shared memory (d = 128): Q 2 x 32 KB, K/V ring 4 x 32 KB, P 32 KB. Every
-// operand is stored as 64-column chunks of 128-byte rows with the 128-byte
-// swizzle, which is what TMA writes and what the MMA descriptors describe.
+// Shared memory: Q 2 x (D/64) x 16 KB and a ring of K/V slots sized to the
+// plan's largest tile. Every operand is stored as 64-column chunks of 128-byte
+// rows with the 128-byte swizzle, which is what TMA writes and what the MMA
+// descriptors describe.
+//
+// Tensor memory (512 columns): S/P buffer 0 at 0, S/P buffer 1 at 128, O at 256.
 #pragma once
 
 #include <cuda.h>
@@ -38,15 +42,15 @@
 
 namespace swa {
 
-constexpr int kTileRows = 128;             // M of every MMA
+constexpr int kTileRows = 128;                // M of every MMA
 constexpr int kChunkBytes = kTileRows * 128;  // one 64-column chunk of a 128-row tile
-constexpr int kPBytes = 2 * kChunkBytes;   // P tile: 128 rows x up to 128 keys, bf16
 constexpr int kTmemCols = 512;
-constexpr int kTmemS0 = 0;                 // S buffers at columns 0 and 128
-constexpr int kTmemO = 256;                // O at columns 256 .. 256 + d
-constexpr int kPrefillThreads = 256;
-constexpr int kSoftmaxWarp0 = 4;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 2^8
+constexpr int kTmemS0 = 0;                    // S/P buffers at columns 0 and 128
+constexpr int kTmemO = 256;                   // O at columns 256 .. 256 + d
+constexpr int kPrefillThreads = 384;
+constexpr int kSoftmaxWarp0 = 4;                // warps 4-11: two softmax warpgroups
+constexpr int kMaxStages = 8;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max grows > 2^8
 
 struct PrefillArgs {
   __nv_bfloat16 *out;
@@ -55,16 +59,139 @@ struct PrefillArgs {
   PrefillPlan plan;
   int n_items;
   int stages;         // K/V ring slots
+  int kv_chunk;       // bytes of one 64-column chunk of a K/V slot
 };
 
+// Shared memory of one CTA.
 template <int D>
 struct PrefillSmem {
-  static constexpr int kQBytes = (D / 64) * kChunkBytes;  // one Q (or K or V) tile
-  static size_t bytes(int stages) {
-    return 1024 /* alignment slack */ + 2 * (size_t)kQBytes + (size_t)stages * kQBytes + kPBytes +
-           256 /* barriers and the TMEM address */;
+  static constexpr int kQBytes = (D / 64) * kChunkBytes;  // one Q tile
+  static constexpr int kBarBytes = 256;
+  // row-max exchange [parity][half][row], then row-sum exchange [half][row]
+  static constexpr int kXchgBytes = (2 * 2 * 128 + 2 * 128) * 4;
+  // keys held by one K/V slot: the largest tile of the plan
+  static int slot_rows(const PrefillPlan &p) { return p.n_band > p.s_box ? p.n_band : p.s_box; }
+  static int chunk_bytes(const PrefillPlan &p) { return slot_rows(p) * 128; }
+  static int slot_bytes(const PrefillPlan &p) { return (D / 64) * chunk_bytes(p); }
+  static size_t fixed_bytes() {
+    return 1024 /* alignment slack */ + 2 * (size_t)kQBytes + kBarBytes + kXchgBytes;
+  }
+  static size_t bytes(const PrefillPlan &p, int stages) {
+    return fixed_bytes() + (size_t)stages * slot_bytes(p);
+  }
+  static int stages(const PrefillPlan &p, int max_smem) {
+    long long st = ((long long)max_smem - (long long)fixed_bytes()) / slot_bytes(p);
+    return (int)(st > kMaxStages ? kMaxStages : st);
   }
 };
+
+// Bit e set iff tile column c0 + e (0 <= e < 16) lies in [lo, hi).
+__device__ __forceinline__ uint32_t range_bits16(int c0, int lo, int hi) {
+  const int l = imin(imax(lo - c0, 0), 16);
+  const int h = imin(imax(hi - c0, 0), 16);
+  return ((1u << h) - 1u) & ~((1u << l) - 1u);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Online-softmax step for this thread's share of one S tile row. Two warps
+// (one per softmax warpgroup) own the same 32 TMEM lanes and split the tile's
+// 16-key chunks: this warp takes NC chunks starting at chunk c_first. Their
+// partial row maxima are exchanged through shared memory, so both apply the
+// same running max. The chunk count is a template parameter so the code is
+// straight-line for each width: no chunk is skipped by predication.
+//   s_row         TMEM address of the row's S values (column 0 of the tile);
+//                 P (bf16, two per column) is written back over them
+//   mask          0: every (row, key) pair of the tile is admitted; otherwise
+//                 the row admits the tile columns [a_lo, a_hi) and
+//                 [b_lo, b_hi) (either range may be empty)
+//   my_max/partner_max  exchange slots of this row; bar_id: named barrier
+//                 shared with the partner warp (64 threads)
+//   m_used        running max (log2 units), identical in both warps
+//   l_part        running sum over this warp's columns
+//   factor        set to the O rescale factor (1: no rescale needed)
+template <int NC>
+__device__ __forceinline__ void softmax_part(uint32_t s_row, int c_first, int mask, int a_lo,
+                                             int a_hi, int b_lo, int b_hi, float cl2,
+                                             float *my_max, const float *partner_max,
+                                             int bar_id, float &m_used, float &l_part,
+                                             float &factor) {
+  constexpr int kN = NC * 16 > 0 ? NC * 16 : 1;
+  float x[kN];
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+    tmem_ld16(s_row + (c_first + c) * 16, *reinterpret_cast<float(*)[16]>(&x[c * 16]));
+  if (NC > 0) tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < NC; ++c) reg_fence16(*reinterpret_cast<float(*)[16]>(&x[c * 16]));
+  if (mask != 0) {
+    // A chunk is masked only when some row of the warp does not admit all of
+    // its 16 keys (the decision is warp-uniform).
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int c0 = (c_first + c) * 16;
+      const uint32_t bits = range_bits16(c0, a_lo, a_hi) | range_bits16(c0, b_lo, b_hi);
+      if (__any_sync(0xffffffffu, bits != 0xFFFFu)) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[c * 16 + e] = (bits >> e) & 1u ? x[c * 16 + e] : -INFINITY;
+      }
+    }
+  }
+  // partial row max of the raw scores, independent chains
+  constexpr int kChains = NC * 16 < 8 ? (NC * 16 > 0 ? NC * 16 : 1) : 8;
+  float mx[kChains];
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) mx[k] = NC > 0 ? x[k] : -INFINITY;
+#pragma unroll
+  for (int e = kChains; e < NC * 16; ++e) mx[e % kChains] = fmaxf(mx[e % kChains], x[e]);
+#pragma unroll
+  for (int k = 1; k < kChains; ++k) mx[0] = fmaxf(mx[0], mx[k]);
+  *my_max = mx[0];
+  named_bar_sync(bar_id, 64);
+  const float m_tile = fmaxf(mx[0], *partner_max) * cl2;  // scale > 0: max commutes with it
+  const float m_new = fmaxf(m_used, m_tile);
+  factor = 1.f;
+  if (m_used == -INFINITY) {
+    m_used = m_new;  // nothing accumulated yet for this row
+  } else if (m_new > m_used + kRescaleThreshold) {
+    factor = fast_exp2(m_used - m_new);
+    m_used = m_new;
+    l_part *= factor;
+  }
+  const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+  float sum[kChains];
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) sum[k] = 0.f;
+  // P = 2^(x * scale * log2 e - m) as bf16: 16 keys -> 8 packed columns
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      x[c * 16 + e] = fast_exp2(fmaf(x[c * 16 + e], cl2, -msub));
+      sum[e % kChains] += x[c * 16 + e];
+    }
+    const float *p = &x[c * 16];
+    tmem_st8(s_row + (c_first + c) * 8, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+             pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]), pack_bf16x2(p[8], p[9]),
+             pack_bf16x2(p[10], p[11]), pack_bf16x2(p[12], p[13]), pack_bf16x2(p[14], p[15]));
+  }
+#pragma unroll
+  for (int k = 1; k < kChains; ++k) sum[0] += sum[k];
+  l_part += sum[0];
+}
+
+// O (+)= P V for one tile of nk (1..8) 16-key steps. The eight MMAs are
+// guarded instead of branched over: the tensor core overlaps consecutive MMAs
+// of a thread only when no branch separates their issue.
+__device__ __forceinline__ void pv_group(int nk, uint32_t accumulate, uint32_t o_tmem,
+                                         uint32_t p_tmem, uint64_t vd, uint32_t idesc) {
+  umma_ts_if(o_tmem, p_tmem, vd, idesc, accumulate, 1u);
+#pragma unroll
+  for (int kk = 1; kk < 8; ++kk)
+    umma_ts_if(o_tmem, p_tmem + kk * 8, vd + kk * 128, idesc, 1u, kk < nk ? 1u : 0u);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
@@ -72,7 +199,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_ks,
-                       const __grid_constant__ CUtensorMap tm_vs, const PrefillArgs a) {
+                       const __grid_constant__ CUtensorMap tm_vs,
+                       const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a) {
   constexpr int kQBytes = PrefillSmem<D>::kQBytes;
   constexpr int kChunks = D / 64;
   constexpr int kSteps = D / 16;  // K steps of the S = Q K^T product
@@ -81,10 +209,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int stages = a.stages;
+  const int kv_chunk = a.kv_chunk;
+  const int slot_bytes = kChunks * kv_chunk;
   uint8_t *sQ = smem;                               // 2 x kQBytes
-  uint8_t *sKV = sQ + 2 * kQBytes;                  // stages x kQBytes
-  uint8_t *sP = sKV + (size_t)stages * kQBytes;     // kPBytes
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sP + kPBytes);
+  uint8_t *sKV = sQ + 2 * kQBytes;                  // stages x slot_bytes
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sKV + (size_t)stages * slot_bytes);
   uint64_t *q_full = bars + 0;      // [2]
   uint64_t *q_empty = bars + 2;     // [2]
   uint64_t *s_full = bars + 4;      // [2]
@@ -94,8 +223,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t *mma_done = bars + 9;    // [1]
   uint64_t *kv_full = bars + 10;    // [stages <= 8]
   uint64_t *kv_empty = bars + 18;   // [stages <= 8]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 27);
+  uint64_t *epi_staged = bars + 26; // [1] output tile staged in shared memory
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 27);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 28);
+  float *xchg = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) +
+                                          PrefillSmem<D>::kBarBytes);  // [2][2][128] + [2][128]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -108,10 +240,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_init(&q_empty[1], 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
     mbar_init(o_full, 1);
     mbar_init(mma_done, 1);
+    mbar_init(epi_staged, 8);
     for (int i = 0; i < stages; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -149,15 +282,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t g = 0;  // global tile counter of this CTA
+      uint32_t u = 0;        // K/V loads issued (two per tile)
+      int slot = 0;          // ring slot of load u
+      uint32_t phase = 0;    // (u / stages) & 1
+      int q_issued = 0;      // Q loads issued (one per item)
       int it = 0;
-      int last_q_parity[2] = {-1, -1};
-      int last_kv_parity[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x, ++it) {
-        const int qb = plan.nqb - 1 - item / BH;
-        const int bh = item % BH;
-        const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+      for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
+           wk.next(), ++it) {
+        const int qb = wk.qb();
+        const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
         const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
         const int qbuf = it & 1;
         if (!mbar_wait(&q_empty[qbuf], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -165,109 +299,175 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int c = 0; c < kChunks; ++c)
           tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
                       kvh * plan.G, bt.t0, b, pol_q);
-        last_q_parity[qbuf] = (it >> 1) & 1;
-        for (int i = 0; i < bt.n_tiles; ++i, ++g) {
+        ++q_issued;
+        for (int i = 0; i < bt.n_tiles; ++i) {
           const Tile tl = tile_at(plan, bt, i, a.w, a.s);
           const int box = tl.sink ? plan.s_box : plan.n_band;
           const uint32_t tile_bytes = (uint32_t)(kChunks * 64 * box * 2);
           for (int half = 0; half < 2; ++half) {  // 0: K, 1: V
-            const uint32_t u = 2 * g + half;
-            const int slot = (int)(u % stages);
-            const uint32_t use = u / stages;
-            if (!mbar_wait(&kv_empty[slot], (use & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&kv_empty[slot], phase ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(&kv_full[slot], tile_bytes);
             const CUtensorMap *tm =
                 half == 0 ? (tl.sink ? &tm_ks : &tm_k) : (tl.sink ? &tm_vs : &tm_v);
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(sKV + slot * kQBytes + c * kChunkBytes, tm, &kv_full[slot], c * 64, kvh,
-                          tl.k0, b, pol_kv);
-            last_kv_parity[slot] = use & 1;
+              tma_load_4d(sKV + slot * slot_bytes + c * kv_chunk, tm, &kv_full[slot], c * 64,
+                          kvh, tl.k0, b, pol_kv);
+            ++u;
+            if (++slot == stages) { slot = 0; phase ^= 1; }
           }
           if (!ok) break;
         }
       }
       if (!ok) {
-        // Let the loads already in flight land before the CTA can exit.
-        for (int i = 0; i < 2; ++i)
-          if (last_q_parity[i] >= 0) mbar_wait(&q_full[i], last_q_parity[i], abort_flag, 200000000ull, false);
-        for (int i = 0; i < stages; ++i)
-          if (last_kv_parity[i] >= 0) mbar_wait(&kv_full[i], last_kv_parity[i], abort_flag, 200000000ull, false);
+        // Let the loads that may still be in flight land before the CTA can
+        // exit: a slot (or Q buffer) is only refilled after its previous load
+        // was consumed, so only the last `stages` K/V loads and the last two Q
+        // loads can be outstanding.
+        const uint32_t first = u > (uint32_t)stages ? u - stages : 0;
+        for (uint32_t v = first; v < u; ++v)
+          mbar_wait(&kv_full[v % stages], (v / stages) & 1, abort_flag, 200000000ull, false);
+        for (int j = q_issued > 2 ? q_issued - 2 : 0; j < q_issued; ++j)
+          mbar_wait(&q_full[j & 1], (j >> 1) & 1, abort_flag, 200000000ull, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      uint32_t g = 0;
-      int it = 0;
-      bool ok = true;
-      // the tile whose S has been issued but whose P V is still pending
-      bool pend = false;
-      uint32_t pend_g = 0;
-      int pend_ncols = 0;
-      bool pend_first = false, pend_last = false;
+    // The whole warp runs the control flow, so descriptors and counters stay
+    // warp-uniform; lane 0 issues each tile's MMAs as one straight-line group
+    // (the tensor core overlaps consecutive MMAs of a thread only when no
+    // branch separates them) followed by its commits. The descriptors are
+    // built once and advanced by adding 16-byte address units, and ring
+    // slots/phases are tracked with counters (no division).
+    const bool leader = lane == 0;
+    auto warp_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      const bool r = mbar_wait(bar, parity, abort_flag);
+      return __all_sync(0xffffffffu, r);
+    };
+    const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+    const uint64_t qd0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t kd0 = sdesc_sw128(smem_u32(sKV), 16, 1024);
+    const uint64_t vd0 = sdesc_sw128(smem_u32(sKV), (uint32_t)kv_chunk, 1024);
+    const uint32_t slot_step = (uint32_t)slot_bytes >> 4;
+    const uint32_t kvc16 = (uint32_t)kv_chunk >> 4;
+    // K of tile g is load 2g, V of tile g is load 2g + 1
+    uint32_t ks = 0, kph = 0;                                        // K slot / phase
+    uint32_t vs = 1 % (uint32_t)stages, vph = 1 / (uint32_t)stages;  // V slot / phase
+    uint32_t g = 0;
+    int it = 0;
+    bool ok = true;
+    // the tile whose S has been issued but whose P V is still pending
+    bool pend = false;
+    uint32_t pend_g = 0, pend_vs = 0, pend_vph = 0;
+    int pend_ncols = 0;
+    bool pend_first = false, pend_last = false;
 
-      auto issue_pv = [&](uint32_t gg, int ncols, bool first, bool last) -> bool {
-        if (!mbar_wait(p_full, gg & 1, abort_flag)) return false;
-        const uint32_t u = 2 * gg + 1;
-        const int slot = (int)(u % stages);
-        if (!mbar_wait(&kv_full[slot], (u / stages) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t v_base = kv_base + slot * kQBytes;
-        for (int kk = 0; kk < ncols / 16; ++kk) {
-          // A = P (K-major, 64-key chunks), B = V (MN-major: d contiguous)
-          const uint64_t adesc = sdesc_sw128(p_base + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(v_base + kk * 2048, kChunkBytes, 1024);
-          umma_bf16_ss(tmem_base + kTmemO, adesc, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&kv_empty[slot]);
+    auto issue_pv = [&]() -> bool {
+      if (!warp_wait(p_full, pend_g & 1)) return false;
+      if (!warp_wait(&kv_full[pend_vs], pend_vph)) return false;
+      tc_fence_after();
+      // A = P (TMEM, 8 columns per 16 keys), B = V (MN-major: d contiguous)
+      const uint32_t p_tmem = tmem_base + kTmemS0 + (pend_g & 1) * 128;
+      const uint64_t vd = vd0 + pend_vs * slot_step;
+      const uint32_t o_tmem = tmem_base + kTmemO;
+      if (leader) {
+        pv_group(pend_ncols >> 4, pend_first ? 0u : 1u, o_tmem, p_tmem, vd, idesc_pv);
+        umma_commit(&kv_empty[pend_vs]);
         umma_commit(pv_done);
-        if (last) umma_commit(o_full);
-        return true;
-      };
-
-      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x, ++it) {
-        const int qb = plan.nqb - 1 - item / BH;
-        const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
-        const int qbuf = it & 1;
-        if (!mbar_wait(&q_full[qbuf], (it >> 1) & 1, abort_flag)) { ok = false; break; }
-        for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-          const Tile tl = tile_at(plan, bt, i, a.w, a.s);
-          const uint32_t u = 2 * g;
-          const int slot = (int)(u % stages);
-          if (!mbar_wait(&kv_full[slot], (u / stages) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t idesc_s = idesc_bf16_f32(128, tl.ncols, false);
-          const uint32_t qa = q_base + qbuf * kQBytes, kb = kv_base + slot * kQBytes;
-#pragma unroll
-          for (int kk = 0; kk < kSteps; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_bf16_ss(tmem_base + kTmemS0 + (g & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
-                         sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&kv_empty[slot]);
-          umma_commit(&s_full[g & 1]);
-          if (i == bt.n_tiles - 1) umma_commit(&q_empty[qbuf]);
-          if (pend && !issue_pv(pend_g, pend_ncols, pend_first, pend_last)) { ok = false; break; }
-          pend = true;
-          pend_g = g;
-          pend_ncols = tl.ncols;
-          pend_first = (i == 0);
-          pend_last = (i == bt.n_tiles - 1);
-        }
+        if (pend_last) umma_commit(o_full);
       }
-      if (ok && pend) issue_pv(pend_g, pend_ncols, pend_first, pend_last);
-      // drain: every MMA issued by this thread completes before TMEM is freed
+      __syncwarp();
+      return true;
+    };
+
+    for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
+         wk.next(), ++it) {
+      // The last P V of the previous block goes first: its epilogue waits
+      // for it, while the first S of this block has the epilogue's duration
+      // to complete.
+      if (pend) {
+        if (!issue_pv()) { ok = false; break; }
+        pend = false;
+      }
+      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const int qbuf = it & 1;
+      const uint64_t qd = qd0 + (uint32_t)qbuf * (uint32_t)(kQBytes >> 4);
+      if (!warp_wait(&q_full[qbuf], (it >> 1) & 1)) { ok = false; break; }
+      for (int i = 0; i < bt.n_tiles; ++i, ++g) {
+        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        if (!warp_wait(&kv_full[ks], kph)) { ok = false; break; }
+        tc_fence_after();
+        // S_g overwrites buffer g % 2, whose P_{g-2} feeds P V_{g-2}: that MMA
+        // was issued before this one and tcgen05 MMAs of one thread execute
+        // in issue order.
+        const uint32_t idesc_s = idesc_bf16_f32(128, tl.ncols, false);
+        const uint32_t s_tmem = tmem_base + kTmemS0 + (g & 1) * 128;
+        const uint64_t kd = kd0 + ks * slot_step;
+        if (leader) {
+          umma_ss<0>(s_tmem, qd, kd, idesc_s);
+#pragma unroll
+          for (int kk = 1; kk < kSteps; ++kk) {
+            const uint32_t qoff = (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2;
+            const uint32_t koff = (kk >> 2) * kvc16 + (kk & 3) * 2;
+            umma_ss<1>(s_tmem, qd + qoff, kd + koff, idesc_s);
+          }
+          umma_commit(&kv_empty[ks]);
+          umma_commit(&s_full[g & 1]);
+        }
+        __syncwarp();
+        if (pend && !issue_pv()) { ok = false; break; }
+        pend = true;
+        pend_g = g;
+        pend_vs = vs;
+        pend_vph = vph;
+        pend_ncols = tl.ncols;
+        pend_first = (i == 0);
+        pend_last = (i == bt.n_tiles - 1);
+        ks += 2;
+        if (ks >= (uint32_t)stages) { ks -= stages; kph ^= 1; }
+        vs += 2;
+        if (vs >= (uint32_t)stages) { vs -= stages; vph ^= 1; }
+      }
+    }
+    if (ok && pend) issue_pv();
+    // drain: every MMA issued by lane 0 completes before TMEM is freed
+    if (leader) {
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, abort_flag, 200000000ull, false);
     }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ output store
+    // The softmax warps stage each finished block, bf16, in the Q buffer it
+    // was computed from (same swizzled layout as the Q tile). This thread
+    // stores it with TMA and then frees the buffer for the next Q load.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_o);
+      int it = 0;
+      for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); wk.valid();
+           wk.next(), ++it) {
+        const int qb = wk.qb();
+        const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
+        const int qbuf = it & 1;
+        if (!mbar_wait(epi_staged, it & 1, abort_flag)) break;
+        for (int c = 0; c < kChunks; ++c)
+          tma_store_4d(&tm_o, sQ + qbuf * kQBytes + c * kChunkBytes, c * 64, kvh * plan.G,
+                       qb * plan.Tq, b);
+        tma_store_commit();
+        tma_store_wait_read();
+        mbar_arrive(&q_empty[qbuf]);
+      }
+      tma_store_wait_all();
+    }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int sub = warp - kSoftmaxWarp0;  // TMEM lane quarter
-    const int r = sub * 32 + lane;         // tile row owned by this thread
+    // Warps 4-7 and 8-11 form two warpgroups. Warp 4 + q and warp 8 + q both
+    // own TMEM lanes 32q .. 32q + 31 (tile rows) and split each tile's
+    // columns: the first warpgroup takes the first ceil(nch / 2) chunks.
+    const int sub = (warp - kSoftmaxWarp0) & 3;   // TMEM lane quarter
+    const int half = (warp - kSoftmaxWarp0) >> 2; // column half
+    const int r = sub * 32 + lane;                // tile row owned by this thread
+    const int bar_id = 1 + sub;                   // named barrier of the warp pair
     const uint32_t lane_addr = tmem_base + ((uint32_t)(sub * 32) << 16);
-    const uint32_t p_row = smem_u32(sP) + r * 128;
     const float cl2 = a.scale_log2;
     // every lane polls; the outcome is made warp-uniform so a timeout on one
     // lane cannot leave the warp diverged before a .sync.aligned instruction
@@ -278,114 +478,67 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x, ++it) {
-      const int qb = plan.nqb - 1 - item / BH;
-      const int bh = item % BH;
-      const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-      const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
-      const int t = bt.t0 + r / plan.G;  // query position of this row
+    const int row_pos = r / plan.G;      // position of this row within a block
+    for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
+         wk.next(), ++it) {
+      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const int t = bt.t0 + row_pos;     // query position of this row
       float m_used = -INFINITY;          // running max (scaled, log2 units)
-      float l_sum = 0.f;
+      float l_part = 0.f;                // sum over this warp's columns
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
         const Tile tl = tile_at(plan, bt, i, a.w, a.s);
         if (!warp_wait(&s_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        float x[128];
-        const uint32_t s_addr = lane_addr + kTmemS0 + (g & 1) * 128;
-        const int nch = tl.ncols >> 4;  // 16-column chunks (ncols is a multiple of 16)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) tmem_ld16(s_addr + c * 16, *reinterpret_cast<float(*)[16]>(&x[c * 16]));
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) reg_fence16(*reinterpret_cast<float(*)[16]>(&x[c * 16]));
+        const uint32_t s_row = lane_addr + kTmemS0 + (g & 1) * 128;
+        // The admitted columns of this row form at most two ranges: the
+        // window part [a_lo, a_hi) and the sink part [b_lo, b_hi) (tile
+        // column indices; either may be empty).
+        int mask = 0, a_lo = 0, a_hi = 0, b_lo = 0, b_hi = 0;
         if (!tl.full) {
-          // The admitted columns of this row form at most two ranges: the
-          // window part [max(own_lo, t-w+1), min(own_hi, t+1)) and the sink
-          // part [own_lo, min(own_hi, s, t+1)).
-          const int a_lo = imax(tl.own_lo, t - a.w + 1) - tl.k0;
-          const int a_hi = imin(tl.own_hi, t + 1) - tl.k0;
-          const int b_lo = tl.own_lo - tl.k0;
-          const int b_hi = imin(imin(tl.own_hi, a.s), t + 1) - tl.k0;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (c < nch) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int col = c * 16 + e;
-                const bool in = (col >= a_lo && col < a_hi) || (col >= b_lo && col < b_hi);
-                x[col] = in ? x[col] : -INFINITY;
-              }
-            }
-        }
-        // row max of the raw scores, eight independent chains
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[c * 16 + e]);
+          mask = 1;
+          a_lo = imax(tl.own_lo, t - a.w + 1) - tl.k0;
+          a_hi = imin(tl.own_hi, t + 1) - tl.k0;
+          if (tl.own_lo < a.s) {  // the tile holds sink keys
+            b_lo = tl.own_lo - tl.k0;
+            b_hi = imin(imin(tl.own_hi, a.s), t + 1) - tl.k0;
           }
-#pragma unroll
-        for (int k = 1; k < 8; ++k) mx8[0] = fmaxf(mx8[0], mx8[k]);
-        const float m_tile = mx8[0] * cl2;  // scale > 0, so the max commutes with it
-        const float m_new = fmaxf(m_used, m_tile);
-        float factor = 1.f;
-        bool rescale = false;
-        if (m_used == -INFINITY) {
-          m_used = m_new;  // nothing accumulated yet for this row
-        } else if (m_new > m_used + kRescaleThreshold) {
-          factor = fast_exp2(m_used - m_new);
-          m_used = m_new;
-          l_sum *= factor;
-          rescale = true;
         }
-        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              x[c * 16 + e] = fast_exp2(fmaf(x[c * 16 + e], cl2, -msub));
-              sum8[e & 7] += x[c * 16 + e];
-            }
-          }
-        float rs = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                   ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        l_sum += rs;
-        // P buffer is free once the previous tile's P V has completed; that
-        // also makes O current for the rescale below.
+        const int nch = tl.ncols >> 4;
+        const int n0 = (nch + 1) >> 1;   // chunks of the first warpgroup
+        const int c_first = half ? n0 : 0;
+        const int my_n = half ? nch - n0 : n0;
+        float *xc = xchg + (g & 1) * 256;
+        float *my_max = xc + half * 128 + r;
+        const float *partner_max = xc + (half ^ 1) * 128 + r;
+        float factor;
+#define SWA_SOFTMAX_PART(N)                                                                  \
+  softmax_part<N>(s_row, c_first, mask, a_lo, a_hi, b_lo, b_hi, cl2, my_max, partner_max, bar_id, \
+                  m_used, l_part, factor)
+        switch (my_n) {
+          case 0: SWA_SOFTMAX_PART(0); break;
+          case 1: SWA_SOFTMAX_PART(1); break;
+          case 2: SWA_SOFTMAX_PART(2); break;
+          case 3: SWA_SOFTMAX_PART(3); break;
+          default: SWA_SOFTMAX_PART(4); break;
+        }
+#undef SWA_SOFTMAX_PART
+        tmem_wait_st();
+        // P V of the previous tile must be complete before O is rescaled (and
+        // it is waited for on every tile so the barrier's phases stay in step).
         if (g > 0 && !warp_wait(pv_done, (g - 1) & 1)) { ok = false; break; }
+        if (__any_sync(0xffffffffu, factor != 1.f)) {
+          // each warp of the pair rescales its half of O's columns
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int u = 2 * c + h;  // 16-byte unit: keys 8u .. 8u+7
-              const uint32_t addr = p_row + (u >> 3) * kChunkBytes + (((u & 7) ^ (r & 7)) << 4);
-              st_shared_v4(addr, pack_bf16x2(x[u * 8 + 0], x[u * 8 + 1]),
-                           pack_bf16x2(x[u * 8 + 2], x[u * 8 + 3]),
-                           pack_bf16x2(x[u * 8 + 4], x[u * 8 + 5]),
-                           pack_bf16x2(x[u * 8 + 6], x[u * 8 + 7]));
-            }
-          }
-        fence_proxy_async_smem();
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             float o[16];
-            tmem_ld16(lane_addr + kTmemO + c * 16, o);
+            const uint32_t oa = lane_addr + kTmemO + half * (D / 2) + c * 16;
+            tmem_ld16(oa, o);
             tmem_wait_ld();
             reg_fence16(o);
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] *= factor;
-            tmem_st16(lane_addr + kTmemO + c * 16, o);
+            tmem_st16(oa, o);
           }
           tmem_wait_st();
         }
@@ -395,33 +548,45 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
+      // O / l -> bf16 into the Q buffer of this block (free: every MMA that
+      // read it completed before O did), in the swizzled layout of the output
+      // tensor map; the store warp writes it out with TMA. Each warp of the
+      // pair converts half of the columns.
+      // (own slots: the partner reads them before it passes the next tile's
+      // barrier, and this warp writes them again only after that)
+      float *xl = xchg + 512;
+      xl[half * 128 + r] = l_part;
+      named_bar_sync(bar_id, 64);
+      const float l_sum = l_part + xl[(half ^ 1) * 128 + r];
       if (!warp_wait(o_full, it & 1)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.0f / l_sum;
-      const bool store = (r < plan.rows) && (t < a.L);
-      __nv_bfloat16 *orow =
-          a.out + (((size_t)b * a.L + t) * a.Hq + (size_t)kvh * plan.G + (r % plan.G)) * D;
+      const uint32_t stage_row = smem_u32(sQ + (it & 1) * kQBytes) + r * 128;
+      float o[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        float o[16];
-        tmem_ld16(lane_addr + kTmemO + c * 16, o);
-        tmem_wait_ld();
-        reg_fence16(o);
-        if (store) {
-          uint4 v0, v1;
-          v0.x = pack_bf16x2(o[0] * inv_l, o[1] * inv_l);
-          v0.y = pack_bf16x2(o[2] * inv_l, o[3] * inv_l);
-          v0.z = pack_bf16x2(o[4] * inv_l, o[5] * inv_l);
-          v0.w = pack_bf16x2(o[6] * inv_l, o[7] * inv_l);
-          v1.x = pack_bf16x2(o[8] * inv_l, o[9] * inv_l);
-          v1.y = pack_bf16x2(o[10] * inv_l, o[11] * inv_l);
-          v1.z = pack_bf16x2(o[12] * inv_l, o[13] * inv_l);
-          v1.w = pack_bf16x2(o[14] * inv_l, o[15] * inv_l);
-          reinterpret_cast<uint4 *>(orow + c * 16)[0] = v0;
-          reinterpret_cast<uint4 *>(orow + c * 16)[1] = v1;
+      for (int j = 0; j < D / 32; ++j)
+        tmem_ld16(lane_addr + kTmemO + half * (D / 2) + j * 16,
+                  *reinterpret_cast<float(*)[16]>(&o[j * 16]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) reg_fence16(*reinterpret_cast<float(*)[16]>(&o[j * 16]));
+      if (r < plan.rows) {
+#pragma unroll
+        for (int u = 0; u < D / 16; ++u) {  // 16-byte unit: 8 columns
+          const int col = half * (D / 2) + u * 8;
+          const int ch = col / 64, unit = (col % 64) / 8;
+          const float *v = &o[u * 8];
+          st_shared_v4(stage_row + ch * kChunkBytes + ((unit ^ (r & 7)) << 4),
+                       pack_bf16x2(v[0] * inv_l, v[1] * inv_l),
+                       pack_bf16x2(v[2] * inv_l, v[3] * inv_l),
+                       pack_bf16x2(v[4] * inv_l, v[5] * inv_l),
+                       pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_staged);
     }
   }
 

@@ -111,12 +111,14 @@ int make_map_bf16_4d(CUtensorMap *map, const void *base, int B, int L, int H, in
 
 // ------------------------------------------------------------------ prefill
 
-int prefill_stages(int d, int max_smem) {
-  const long long qb = (long long)(d / 64) * swa::kChunkBytes;
-  const long long fixed = 1024 + 256 + 2 * qb + swa::kPBytes;
-  long long st = (max_smem - fixed) / qb;
-  if (st > 8) st = 8;
-  return (int)st;
+int prefill_stages(int d, const swa::PrefillPlan &plan, int max_smem) {
+  return d == 64 ? swa::PrefillSmem<64>::stages(plan, max_smem)
+                 : swa::PrefillSmem<128>::stages(plan, max_smem);
+}
+
+size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages) {
+  return d == 64 ? swa::PrefillSmem<64>::bytes(plan, stages)
+                 : swa::PrefillSmem<128>::bytes(plan, stages);
 }
 
 template <int D>
@@ -124,9 +126,10 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
                    int Hkv, int w, int s, float scale, cudaStream_t stream,
                    const DeviceInfo &dev) {
   const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
-  CUtensorMap tq, tk, tv, tks, tvs;
+  CUtensorMap tq, tk, tv, tks, tvs, to;
   int rc;
   if ((rc = make_map_bf16_4d(&tq, q, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+  if ((rc = make_map_bf16_4d(&to, out, B, L, Hq, D, plan.G, plan.Tq))) return rc;
   if ((rc = make_map_bf16_4d(&tk, k, B, L, Hkv, D, 1, plan.n_band))) return rc;
   if ((rc = make_map_bf16_4d(&tv, v, B, L, Hkv, D, 1, plan.n_band))) return rc;
   if (plan.n_sink > 0) {
@@ -136,9 +139,9 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
     tks = tk;
     tvs = tv;
   }
-  const int stages = prefill_stages(D, dev.max_smem_optin);
+  const int stages = prefill_stages(D, plan, dev.max_smem_optin);
   if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
-  const size_t smem = swa::PrefillSmem<D>::bytes(stages);
+  const size_t smem = swa::PrefillSmem<D>::bytes(plan, stages);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -160,8 +163,10 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.plan = plan;
   a.n_items = B * Hkv * plan.nqb;
   a.stages = stages;
+  a.kv_chunk = swa::PrefillSmem<D>::chunk_bytes(plan);
   const int grid = swa::imin(a.n_items, dev.sms);
-  swa::swa_prefill_kernel<D><<<grid, swa::kPrefillThreads, smem, stream>>>(tq, tk, tv, tks, tvs, a);
+  swa::swa_prefill_kernel<D><<<grid, swa::kPrefillThreads, smem, stream>>>(tq, tk, tv, tks, tvs, to,
+                                                                         a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "swa_prefill launch");
   return SWA_OK;
@@ -298,16 +303,16 @@ int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]) {
   plan[2] = p.n_band;
   plan[3] = p.s_box;
   plan[4] = p.n_sink;
-  plan[5] = prefill_stages(d, 232448);
+  plan[5] = prefill_stages(d, p, 232448);
   plan[6] = 0;
-  plan[7] = 0;
+  plan[7] = (int)prefill_smem_bytes(d, p, plan[5]);
   int dev_count = 0;
   if (cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0) {
     DeviceInfo dev;
     if (current_device_info(&dev) == SWA_OK) {
-      plan[5] = prefill_stages(d, dev.max_smem_optin);
+      plan[5] = prefill_stages(d, p, dev.max_smem_optin);
       plan[6] = dev.sms;
-      plan[7] = (int)(d == 64 ? swa::PrefillSmem<64>::bytes(plan[5]) : swa::PrefillSmem<128>::bytes(plan[5]));
+      plan[7] = (int)prefill_smem_bytes(d, p, plan[5]);
     }
   } else {
     cudaGetLastError();

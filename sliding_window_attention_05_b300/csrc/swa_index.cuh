@@ -57,7 +57,23 @@ struct PrefillPlan {
   int s_box;      // keys per sink tile (multiple of 16, <= 128), 0 if s == 0
   int n_sink;     // sink tiles per block, 0 if s == 0
   int nqb;        // query blocks per (batch, KV head)
+  float inv_band; // 1 / n_band (device-side division by n_band)
 };
+
+// ceil(x / p.n_band) for x >= 0. Below 2^22 the device path multiplies by
+// the float reciprocal and corrects the quotient by one step either way.
+SWA_HD int cdiv_band(const PrefillPlan &p, int x) {
+#if defined(__CUDA_ARCH__)
+  const int y = x + p.n_band - 1;
+  if (y >= (1 << 22)) return y / p.n_band;
+  int q = (int)((float)y * p.inv_band);
+  if (q * p.n_band > y) --q;
+  if ((q + 1) * p.n_band <= y) ++q;
+  return q;
+#else
+  return cdiv(x, p.n_band);
+#endif
+}
 
 SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
   PrefillPlan p;
@@ -71,6 +87,7 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
   if (span > L) span = L;
   int nt = (int)((span + 127) / 128);
   p.n_band = imin(128, round_up(cdiv((int)span, nt), 16));
+  p.inv_band = 1.0f / (float)p.n_band;
   if (s > 0) {
     p.n_sink = cdiv(s, 128);
     p.s_box = imin(128, round_up(cdiv(s, p.n_sink), 16));
@@ -104,9 +121,38 @@ SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s)
     if (s > 0) lo = 0;             // window reaches the sinks: one merged range
   }
   b.lo = lo;
-  b.n_tiles = b.n_sink + cdiv(b.t_last - lo + 1, p.n_band);
+  b.n_tiles = b.n_sink + cdiv_band(p, b.t_last - lo + 1);
   return b;
 }
+
+// The work items of one persistent CTA: item = first, first + stride, ...
+// Each item is a query block qb of one (batch, KV head) pair bh, with
+// item = (nqb - 1 - qb) * BH + bh, so the longest blocks of a causal prompt
+// come first. Advancing costs no division.
+struct ItemWalker {
+  int item, stride, n_items, BH, nqb;
+  int q, rem;    // item / BH, item % BH
+  int sq, sr;    // stride / BH, stride % BH
+  SWA_HD ItemWalker(int first, int stride_, int n_items_, int BH_, int nqb_)
+      : item(first), stride(stride_), n_items(n_items_), BH(BH_), nqb(nqb_) {
+    q = first / BH;
+    rem = first % BH;
+    sq = stride / BH;
+    sr = stride % BH;
+  }
+  SWA_HD bool valid() const { return item < n_items; }
+  SWA_HD int qb() const { return nqb - 1 - q; }
+  SWA_HD int bh() const { return rem; }
+  SWA_HD void next() {
+    item += stride;
+    q += sq;
+    rem += sr;
+    if (rem >= BH) {
+      rem -= BH;
+      ++q;
+    }
+  }
+};
 
 struct Tile {
   int k0;        // first key row loaded
