@@ -138,8 +138,8 @@ SWA_API size_t swa_cache_bytes(int B, int Hkv, int d, int w, int s);
 
 /* Host helper: the prefill tiling the library picks for these sizes.
  * plan[0] query positions per block (Tq)      plan[1] tile rows (Tq * Hq/Hkv)
- * plan[2] keys per band tile                  plan[3] keys per sink tile (0: none)
- * plan[4] sink tiles per block                plan[5] K/V pipeline stages
+ * plan[2] keys per band tile (<= 192)         plan[3] keys per sink box (0: none)
+ * plan[4] sink boxes (ceil(s / 128))          plan[5] K/V pipeline stages
  * plan[6] persistent CTAs on the current device (0 without a device)
  * plan[7] dynamic shared memory bytes per CTA */
 SWA_API int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]);

@@ -321,9 +321,11 @@ __global__ void swa_keymask_kernel(PrefillPlan plan, int L, int w, int s, int ro
   int local = 0;
   for (int i = 0; i < bt.n_tiles; ++i) {
     const Tile tl = tile_at(plan, bt, i, w, s);
+    // the same column ranges the prefill softmax keeps unmasked
+    const ColRanges cr = tile_ranges(tl, t, w, s);
     for (int c = threadIdx.x; c < tl.ncols; c += blockDim.x) {
-      const int j = tl.k0 + c;
-      const bool ok = tl.full || admit(t, j, w, s, tl.own_lo, tl.own_hi);
+      const int j = tile_key(tl, c);
+      const bool ok = tl.full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
       if (ok && j >= 0 && j < L) {
         atomicOr(&row_bits[j / 32], 1u << (j % 32));
         ++local;

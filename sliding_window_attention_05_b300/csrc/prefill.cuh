@@ -30,7 +30,7 @@
 // rows with the 128-byte swizzle, which is what TMA writes and what the MMA
 // descriptors describe.
 //
-// Tensor memory (512 columns): S/P buffer 0 at 0, S/P buffer 1 at 128, O at 256.
+// Tensor memory (512 columns): S/P buffer 0 at 0, S/P buffer 1 at 192, O at 384.
 #pragma once
 
 #include <cuda.h>
@@ -45,8 +45,9 @@ namespace swa {
 constexpr int kTileRows = 128;                // M of every MMA
 constexpr int kChunkBytes = kTileRows * 128;  // one 64-column chunk of a 128-row tile
 constexpr int kTmemCols = 512;
-constexpr int kTmemS0 = 0;                    // S/P buffers at columns 0 and 128
-constexpr int kTmemO = 256;                   // O at columns 256 .. 256 + d
+constexpr int kTmemS0 = 0;                    // S/P buffers at columns 0 and 192
+constexpr int kTmemSStride = kMaxTileKeys;
+constexpr int kTmemO = 2 * kMaxTileKeys;      // O at columns 384 .. 384 + d
 constexpr int kPrefillThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;                // warps 4-11: two softmax warpgroups
 constexpr int kMaxStages = 8;
@@ -60,6 +61,9 @@ struct PrefillArgs {
   int n_items;
   int stages;         // K/V ring slots
   int kv_chunk;       // bytes of one 64-column chunk of a K/V slot
+  int sep_stage;      // 1: the output is staged in a buffer of its own, so a Q
+                      // buffer is free as soon as its block's last S is done;
+                      // 0: the output is staged in the block's Q buffer
 };
 
 // Shared memory of one CTA.
@@ -69,19 +73,25 @@ struct PrefillSmem {
   static constexpr int kBarBytes = 256;
   // row-max exchange [parity][half][row], then row-sum exchange [half][row]
   static constexpr int kXchgBytes = (2 * 2 * 128 + 2 * 128) * 4;
-  // keys held by one K/V slot: the largest tile of the plan
-  static int slot_rows(const PrefillPlan &p) { return p.n_band > p.s_box ? p.n_band : p.s_box; }
-  static int chunk_bytes(const PrefillPlan &p) { return slot_rows(p) * 128; }
+  // keys held by one K/V slot: the widest tile of the plan
+  static int chunk_bytes(const PrefillPlan &p) { return p.slot_keys * 128; }
   static int slot_bytes(const PrefillPlan &p) { return (D / 64) * chunk_bytes(p); }
-  static size_t fixed_bytes() {
-    return 1024 /* alignment slack */ + 2 * (size_t)kQBytes + kBarBytes + kXchgBytes;
+  static size_t fixed_bytes(bool sep_stage) {
+    return 1024 /* alignment slack */ + (sep_stage ? 3 : 2) * (size_t)kQBytes + kBarBytes +
+           kXchgBytes;
   }
-  static size_t bytes(const PrefillPlan &p, int stages) {
-    return fixed_bytes() + (size_t)stages * slot_bytes(p);
+  static size_t bytes(const PrefillPlan &p, int stages, bool sep_stage) {
+    return fixed_bytes(sep_stage) + (size_t)stages * slot_bytes(p);
   }
-  static int stages(const PrefillPlan &p, int max_smem) {
-    long long st = ((long long)max_smem - (long long)fixed_bytes()) / slot_bytes(p);
+  static int stages(const PrefillPlan &p, int max_smem, bool sep_stage) {
+    long long st = ((long long)max_smem - (long long)fixed_bytes(sep_stage)) / slot_bytes(p);
     return (int)(st > kMaxStages ? kMaxStages : st);
+  }
+  // A separate output buffer is used when the K/V ring still keeps enough
+  // stages: two (the K and V of the one tile) when a block visits a single
+  // tile, four otherwise.
+  static bool use_sep_stage(const PrefillPlan &p, int max_smem) {
+    return stages(p, max_smem, true) >= (p.steady_tiles == 1 ? 2 : 4);
   }
 };
 
@@ -182,14 +192,14 @@ __device__ __forceinline__ void softmax_part(uint32_t s_row, int c_first, int ma
   l_part += sum[0];
 }
 
-// O (+)= P V for one tile of nk (1..8) 16-key steps. The eight MMAs are
-// guarded instead of branched over: the tensor core overlaps consecutive MMAs
-// of a thread only when no branch separates their issue.
+// O (+)= P V for one tile of nk (1 .. kMaxTileKeys / 16) 16-key steps. The
+// MMAs are guarded instead of branched over: the tensor core overlaps
+// consecutive MMAs of a thread only when no branch separates their issue.
 __device__ __forceinline__ void pv_group(int nk, uint32_t accumulate, uint32_t o_tmem,
                                          uint32_t p_tmem, uint64_t vd, uint32_t idesc) {
   umma_ts_if(o_tmem, p_tmem, vd, idesc, accumulate, 1u);
 #pragma unroll
-  for (int kk = 1; kk < 8; ++kk)
+  for (int kk = 1; kk < kMaxTileKeys / 16; ++kk)
     umma_ts_if(o_tmem, p_tmem + kk * 8, vd + kk * 128, idesc, 1u, kk < nk ? 1u : 0u);
 }
 
@@ -212,7 +222,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int kv_chunk = a.kv_chunk;
   const int slot_bytes = kChunks * kv_chunk;
   uint8_t *sQ = smem;                               // 2 x kQBytes
-  uint8_t *sKV = sQ + 2 * kQBytes;                  // stages x slot_bytes
+  uint8_t *sStage = a.sep_stage ? sQ + 2 * kQBytes : nullptr;  // kQBytes (optional)
+  uint8_t *sKV = sQ + (a.sep_stage ? 3 : 2) * kQBytes;        // stages x slot_bytes
   uint64_t *bars = reinterpret_cast<uint64_t *>(sKV + (size_t)stages * slot_bytes);
   uint64_t *q_full = bars + 0;      // [2]
   uint64_t *q_empty = bars + 2;     // [2]
@@ -224,6 +235,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t *kv_full = bars + 10;    // [stages <= 8]
   uint64_t *kv_empty = bars + 18;   // [stages <= 8]
   uint64_t *epi_staged = bars + 26; // [1] output tile staged in shared memory
+  uint64_t *stage_free = bars + 29; // [1] separate staging buffer read by TMA
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 27);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 28);
   float *xchg = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) +
@@ -245,6 +257,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_init(o_full, 1);
     mbar_init(mma_done, 1);
     mbar_init(epi_staged, 8);
+    mbar_init(stage_free, 1);
     for (int i = 0; i < stages; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -294,24 +307,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
         const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
         const int qbuf = it & 1;
-        if (!mbar_wait(&q_empty[qbuf], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)(kChunks * 64 * plan.rows * 2));
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
-                      kvh * plan.G, bt.t0, b, pol_q);
-        ++q_issued;
+        // Order of loads: K of the first tile, Q, then the rest. That K's ring
+        // slot frees up when an earlier block's S is done, while the Q buffer
+        // may wait for an earlier block; Q must precede every V load, since a
+        // V slot frees up only after a P V that the MMA warp issues after the
+        // next S, which needs this Q.
         for (int i = 0; i < bt.n_tiles; ++i) {
           const Tile tl = tile_at(plan, bt, i, a.w, a.s);
-          const int box = tl.sink ? plan.s_box : plan.n_band;
-          const uint32_t tile_bytes = (uint32_t)(kChunks * 64 * box * 2);
+          // slot rows [0, n_sink_cols): the sink box; then the band box
+          const bool band = tl.ncols > tl.n_sink_cols;
+          const uint32_t tile_bytes =
+              (uint32_t)(kChunks * 128 * (tl.n_sink_cols + (band ? plan.n_band : 0)));
           for (int half = 0; half < 2; ++half) {  // 0: K, 1: V
+            if (i == 0 && half == 1) {
+              if (!mbar_wait(&q_empty[qbuf], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+              mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)(kChunks * 64 * plan.rows * 2));
+              for (int c = 0; c < kChunks; ++c)
+                tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
+                            kvh * plan.G, bt.t0, b, pol_q);
+              ++q_issued;
+            }
             if (!mbar_wait(&kv_empty[slot], phase ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(&kv_full[slot], tile_bytes);
-            const CUtensorMap *tm =
-                half == 0 ? (tl.sink ? &tm_ks : &tm_k) : (tl.sink ? &tm_vs : &tm_v);
-            for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(sKV + slot * slot_bytes + c * kv_chunk, tm, &kv_full[slot], c * 64,
-                          kvh, tl.k0, b, pol_kv);
+            uint8_t *dst = sKV + slot * slot_bytes;
+            for (int c = 0; c < kChunks; ++c) {
+              if (tl.n_sink_cols)
+                tma_load_4d(dst + c * kv_chunk, half == 0 ? &tm_ks : &tm_vs, &kv_full[slot],
+                            c * 64, kvh, tl.sink_key0, b, pol_kv);
+              if (band)
+                tma_load_4d(dst + c * kv_chunk + tl.n_sink_cols * 128, half == 0 ? &tm_k : &tm_v,
+                            &kv_full[slot], c * 64, kvh, tl.k0, b, pol_kv);
+            }
             ++u;
             if (++slot == stages) { slot = 0; phase ^= 1; }
           }
@@ -366,7 +392,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!warp_wait(&kv_full[pend_vs], pend_vph)) return false;
       tc_fence_after();
       // A = P (TMEM, 8 columns per 16 keys), B = V (MN-major: d contiguous)
-      const uint32_t p_tmem = tmem_base + kTmemS0 + (pend_g & 1) * 128;
+      const uint32_t p_tmem = tmem_base + kTmemS0 + (pend_g & 1) * kTmemSStride;
       const uint64_t vd = vd0 + pend_vs * slot_step;
       const uint32_t o_tmem = tmem_base + kTmemO;
       if (leader) {
@@ -381,13 +407,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
          wk.next(), ++it) {
-      // The last P V of the previous block goes first: its epilogue waits
-      // for it, while the first S of this block has the epilogue's duration
-      // to complete.
-      if (pend) {
-        if (!issue_pv()) { ok = false; break; }
-        pend = false;
-      }
       const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
       const int qbuf = it & 1;
       const uint64_t qd = qd0 + (uint32_t)qbuf * (uint32_t)(kQBytes >> 4);
@@ -396,11 +415,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const Tile tl = tile_at(plan, bt, i, a.w, a.s);
         if (!warp_wait(&kv_full[ks], kph)) { ok = false; break; }
         tc_fence_after();
-        // S_g overwrites buffer g % 2, whose P_{g-2} feeds P V_{g-2}: that MMA
-        // was issued before this one and tcgen05 MMAs of one thread execute
-        // in issue order.
+        // S_g is issued before P V_{g-1} (which needs the softmax of tile g - 1),
+        // also across blocks, so the tensor core computes S_g while the
+        // softmax warps still work on tile g - 1. S_g overwrites buffer g % 2,
+        // whose P_{g-2} feeds P V_{g-2}: that MMA was issued before this one
+        // and tcgen05 MMAs of one thread execute in issue order.
         const uint32_t idesc_s = idesc_bf16_f32(128, tl.ncols, false);
-        const uint32_t s_tmem = tmem_base + kTmemS0 + (g & 1) * 128;
+        const uint32_t s_tmem = tmem_base + kTmemS0 + (g & 1) * kTmemSStride;
         const uint64_t kd = kd0 + ks * slot_step;
         if (leader) {
           umma_ss<0>(s_tmem, qd, kd, idesc_s);
@@ -412,6 +433,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
           umma_commit(&kv_empty[ks]);
           umma_commit(&s_full[g & 1]);
+          if (a.sep_stage && i == bt.n_tiles - 1) umma_commit(&q_empty[qbuf]);
         }
         __syncwarp();
         if (pend && !issue_pv()) { ok = false; break; }
@@ -449,12 +471,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
         const int qbuf = it & 1;
         if (!mbar_wait(epi_staged, it & 1, abort_flag)) break;
+        const uint8_t *src = a.sep_stage ? sStage : sQ + qbuf * kQBytes;
         for (int c = 0; c < kChunks; ++c)
-          tma_store_4d(&tm_o, sQ + qbuf * kQBytes + c * kChunkBytes, c * 64, kvh * plan.G,
-                       qb * plan.Tq, b);
+          tma_store_4d(&tm_o, src + c * kChunkBytes, c * 64, kvh * plan.G, qb * plan.Tq, b);
         tma_store_commit();
         tma_store_wait_read();
-        mbar_arrive(&q_empty[qbuf]);
+        mbar_arrive(a.sep_stage ? stage_free : &q_empty[qbuf]);
       }
       tma_store_wait_all();
     }
@@ -489,19 +511,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const Tile tl = tile_at(plan, bt, i, a.w, a.s);
         if (!warp_wait(&s_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_row = lane_addr + kTmemS0 + (g & 1) * 128;
-        // The admitted columns of this row form at most two ranges: the
-        // window part [a_lo, a_hi) and the sink part [b_lo, b_hi) (tile
-        // column indices; either may be empty).
-        int mask = 0, a_lo = 0, a_hi = 0, b_lo = 0, b_hi = 0;
+        const uint32_t s_row = lane_addr + kTmemS0 + (g & 1) * kTmemSStride;
+        int mask = 0;
+        ColRanges cr{0, 0, 0, 0};
         if (!tl.full) {
           mask = 1;
-          a_lo = imax(tl.own_lo, t - a.w + 1) - tl.k0;
-          a_hi = imin(tl.own_hi, t + 1) - tl.k0;
-          if (tl.own_lo < a.s) {  // the tile holds sink keys
-            b_lo = tl.own_lo - tl.k0;
-            b_hi = imin(imin(tl.own_hi, a.s), t + 1) - tl.k0;
-          }
+          cr = tile_ranges(tl, t, a.w, a.s);
         }
         const int nch = tl.ncols >> 4;
         const int n0 = (nch + 1) >> 1;   // chunks of the first warpgroup
@@ -512,14 +527,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const float *partner_max = xc + (half ^ 1) * 128 + r;
         float factor;
 #define SWA_SOFTMAX_PART(N)                                                                  \
-  softmax_part<N>(s_row, c_first, mask, a_lo, a_hi, b_lo, b_hi, cl2, my_max, partner_max, bar_id, \
-                  m_used, l_part, factor)
+  softmax_part<N>(s_row, c_first, mask, cr.a_lo, cr.a_hi, cr.b_lo, cr.b_hi, cl2, my_max,      \
+                  partner_max, bar_id, m_used, l_part, factor)
         switch (my_n) {
           case 0: SWA_SOFTMAX_PART(0); break;
           case 1: SWA_SOFTMAX_PART(1); break;
           case 2: SWA_SOFTMAX_PART(2); break;
           case 3: SWA_SOFTMAX_PART(3); break;
-          default: SWA_SOFTMAX_PART(4); break;
+          case 4: SWA_SOFTMAX_PART(4); break;
+          case 5: SWA_SOFTMAX_PART(5); break;
+          default: SWA_SOFTMAX_PART(6); break;
         }
 #undef SWA_SOFTMAX_PART
         tmem_wait_st();
@@ -559,9 +576,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       named_bar_sync(bar_id, 64);
       const float l_sum = l_part + xl[(half ^ 1) * 128 + r];
       if (!warp_wait(o_full, it & 1)) { ok = false; break; }
+      // a separate staging buffer is free once the previous block's store read it
+      if (a.sep_stage && !warp_wait(stage_free, (it & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.0f / l_sum;
-      const uint32_t stage_row = smem_u32(sQ + (it & 1) * kQBytes) + r * 128;
+      const uint32_t stage_row =
+          smem_u32(a.sep_stage ? sStage : sQ + (it & 1) * kQBytes) + r * 128;
       float o[D / 2];
 #pragma unroll
       for (int j = 0; j < D / 32; ++j)

@@ -66,14 +66,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after
-// timeout_ns (or, when `abortable`, as soon as another role has set *abort),
-// records the error and returns false; never spins forever. Drain waits at
-// kernel exit pass abortable = false so in-flight copies and MMAs still land.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint64_t timeout_ns = 2000000000ull,
-                                          bool abortable = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait (kept out of line: it is rarely taken, and a copy at
+// every wait would crowd the instruction cache).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                            uint64_t timeout_ns, bool abortable) {
   const uint64_t t0 = global_timer_ns();
   uint32_t it = 0;
   while (true) {
@@ -87,6 +83,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Wait for the phase with the given parity to complete. Gives up after
+// timeout_ns (or, when `abortable`, as soon as another role has set *abort),
+// records the error and returns false; never spins forever. Drain waits at
+// kernel exit pass abortable = false so in-flight copies and MMAs still land.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t timeout_ns = 2000000000ull,
+                                          bool abortable = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, timeout_ns, abortable);
 }
 
 // ---------------------------------------------------------------- proxies

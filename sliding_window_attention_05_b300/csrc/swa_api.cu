@@ -111,14 +111,20 @@ int make_map_bf16_4d(CUtensorMap *map, const void *base, int B, int L, int H, in
 
 // ------------------------------------------------------------------ prefill
 
-int prefill_stages(int d, const swa::PrefillPlan &plan, int max_smem) {
-  return d == 64 ? swa::PrefillSmem<64>::stages(plan, max_smem)
-                 : swa::PrefillSmem<128>::stages(plan, max_smem);
+bool prefill_sep_stage(int d, const swa::PrefillPlan &plan, int max_smem) {
+  return d == 64 ? swa::PrefillSmem<64>::use_sep_stage(plan, max_smem)
+                 : swa::PrefillSmem<128>::use_sep_stage(plan, max_smem);
 }
 
-size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages) {
-  return d == 64 ? swa::PrefillSmem<64>::bytes(plan, stages)
-                 : swa::PrefillSmem<128>::bytes(plan, stages);
+int prefill_stages(int d, const swa::PrefillPlan &plan, int max_smem) {
+  const bool sep = prefill_sep_stage(d, plan, max_smem);
+  return d == 64 ? swa::PrefillSmem<64>::stages(plan, max_smem, sep)
+                 : swa::PrefillSmem<128>::stages(plan, max_smem, sep);
+}
+
+size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages, bool sep) {
+  return d == 64 ? swa::PrefillSmem<64>::bytes(plan, stages, sep)
+                 : swa::PrefillSmem<128>::bytes(plan, stages, sep);
 }
 
 template <int D>
@@ -139,9 +145,10 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
     tks = tk;
     tvs = tv;
   }
+  const bool sep_stage = prefill_sep_stage(D, plan, dev.max_smem_optin);
   const int stages = prefill_stages(D, plan, dev.max_smem_optin);
   if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
-  const size_t smem = swa::PrefillSmem<D>::bytes(plan, stages);
+  const size_t smem = swa::PrefillSmem<D>::bytes(plan, stages, sep_stage);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -164,6 +171,7 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.n_items = B * Hkv * plan.nqb;
   a.stages = stages;
   a.kv_chunk = swa::PrefillSmem<D>::chunk_bytes(plan);
+  a.sep_stage = sep_stage ? 1 : 0;
   const int grid = swa::imin(a.n_items, dev.sms);
   swa::swa_prefill_kernel<D><<<grid, swa::kPrefillThreads, smem, stream>>>(tq, tk, tv, tks, tvs, to,
                                                                          a);
@@ -305,14 +313,14 @@ int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]) {
   plan[4] = p.n_sink;
   plan[5] = prefill_stages(d, p, 232448);
   plan[6] = 0;
-  plan[7] = (int)prefill_smem_bytes(d, p, plan[5]);
+  plan[7] = (int)prefill_smem_bytes(d, p, plan[5], prefill_sep_stage(d, p, 232448));
   int dev_count = 0;
   if (cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0) {
     DeviceInfo dev;
     if (current_device_info(&dev) == SWA_OK) {
       plan[5] = prefill_stages(d, p, dev.max_smem_optin);
       plan[6] = dev.sms;
-      plan[7] = (int)prefill_smem_bytes(d, p, plan[5]);
+      plan[7] = (int)prefill_smem_bytes(d, p, plan[5], prefill_sep_stage(d, p, dev.max_smem_optin));
     }
   } else {
     cudaGetLastError();
@@ -475,9 +483,12 @@ int swa_keymask_host(int L, int Hq, int Hkv, int d, int w, int s, int row0, int 
     const swa::BlockTiles bt = swa::block_tiles(plan, t / plan.Tq, L, w, s);
     for (int i = 0; i < bt.n_tiles; ++i) {
       const swa::Tile tl = swa::tile_at(plan, bt, i, w, s);
+      const swa::ColRanges cr = swa::tile_ranges(tl, t, w, s);
       for (int c = 0; c < tl.ncols; ++c) {
-        const int j = tl.k0 + c;
-        if ((tl.full || swa::admit(t, j, w, s, tl.own_lo, tl.own_hi)) && j >= 0 && j < L) {
+        const int j = swa::tile_key(tl, c);
+        const bool ok =
+            tl.full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
+        if (ok && j >= 0 && j < L) {
           row_bits[j / 32] |= 1u << (j % 32);
           ++cnt;
         }

@@ -49,13 +49,25 @@ SWA_HD bool admit(int t, int j, int w, int s, int own_lo, int own_hi) {
 // the M = 128 rows of one tensor-core tile (row r <-> position t0 + r / G,
 // head kvh * G + r % G). Packing the group shrinks the key span a block needs
 // from (w + 127) to (w + Tq - 1) keys.
+//
+// A block visits a short list of key tiles (at most kMaxTileKeys keys each,
+// the MMA's N): its band tiles, which cover the window part of every row, and
+// the sink keys. The sinks ride in the first band tile (a second TMA box in
+// the same shared-memory slot) when that tile has room, otherwise they form
+// tiles of their own. Every tile not listed is skipped: no load, no MMA, no
+// exponential.
+constexpr int kMaxTileKeys = 192;
+
 struct PrefillPlan {
   int G;          // query heads per KV head
   int Tq;         // query positions per block
   int rows;       // Tq * G <= 128 (rows past this stay zero)
-  int n_band;     // keys per band tile (multiple of 16, <= 128)
-  int s_box;      // keys per sink tile (multiple of 16, <= 128), 0 if s == 0
-  int n_sink;     // sink tiles per block, 0 if s == 0
+  int n_band;     // keys per band tile (multiple of 16, <= kMaxTileKeys)
+  int s_box;      // keys per sink box (multiple of 16, <= 128), 0 if s == 0
+  int n_sink;     // sink boxes, ceil(s / 128); 0 if s == 0
+  int merge;      // 1: the (single) sink box rides in the first band tile
+  int slot_keys;  // keys one K/V ring slot holds: the widest tile
+  int steady_tiles;  // tiles a block far from the sequence start visits
   int nqb;        // query blocks per (batch, KV head)
   float inv_band; // 1 / n_band (device-side division by n_band)
 };
@@ -82,12 +94,15 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
   p.rows = p.Tq * p.G;
   p.nqb = cdiv(L, p.Tq);
   // Band tiles: spread the steady-state span (w + Tq - 1 keys) evenly over the
-  // fewest tiles of at most 128 keys, rounded up to the MMA's N granularity.
+  // fewest tiles of at most kMaxTileKeys keys, rounded up to the MMA's N
+  // granularity of 16.
   long long span = (long long)imin(w, L) + p.Tq - 1;
   if (span > L) span = L;
-  int nt = (int)((span + 127) / 128);
-  p.n_band = imin(128, round_up(cdiv((int)span, nt), 16));
-  p.inv_band = 1.0f / (float)p.n_band;
+  // Tile widths are kept to multiples of 32 keys so that the two softmax
+  // warps sharing a row take equal halves of every tile (and run the same
+  // code).
+  const int nt = (int)((span + kMaxTileKeys - 1) / kMaxTileKeys);
+  p.n_band = imin(kMaxTileKeys, round_up(cdiv((int)span, nt), 32));
   if (s > 0) {
     p.n_sink = cdiv(s, 128);
     p.s_box = imin(128, round_up(cdiv(s, p.n_sink), 16));
@@ -95,18 +110,23 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
     p.n_sink = 0;
     p.s_box = 0;
   }
+  p.merge = (p.n_sink == 1 && round_up(p.s_box + p.n_band, 32) <= kMaxTileKeys) ? 1 : 0;
+  if (p.merge) p.n_band = round_up(p.s_box + p.n_band, 32) - p.s_box;
+  p.inv_band = 1.0f / (float)p.n_band;
+  p.steady_tiles = (p.merge ? 0 : p.n_sink) + cdiv((int)span, p.n_band);
+  p.slot_keys = p.merge ? p.s_box + p.n_band : imax(p.n_band, p.s_box);
   return p;
 }
 
-// The tiles one query block visits: optional sink tiles first (so the running
-// maximum is seen early), then band tiles that cover [lo, t_last]. Every tile
-// not listed is skipped: no load, no MMA, no exponential.
+// The tiles one query block visits: tiles of sink boxes first (when the sinks
+// do not ride in the first band tile), then band tiles that cover [lo, t_last].
 struct BlockTiles {
-  int t0;        // first query position of the block
-  int t_last;    // last valid query position (< L)
-  int lo;        // first key of the band part
-  int n_sink;    // separate sink tiles (0 when the window reaches the sinks)
-  int n_tiles;   // sink tiles + band tiles
+  int t0;          // first query position of the block
+  int t_last;      // last valid query position (< L)
+  int lo;          // first key of the band part
+  int n_sink;      // tiles made of sink boxes only
+  int sink_first;  // 1: the first band tile also carries the sink box
+  int n_tiles;     // all tiles
 };
 
 SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s) {
@@ -114,11 +134,15 @@ SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s)
   b.t0 = qb * p.Tq;
   b.t_last = imin(b.t0 + p.Tq, L) - 1;
   int lo = imax(0, b.t0 - w + 1);  // leftmost window key of any row in the block
-  if (s > 0 && lo >= s) {
-    b.n_sink = p.n_sink;           // sinks lie left of every row's window
-  } else {
-    b.n_sink = 0;
-    if (s > 0) lo = 0;             // window reaches the sinks: one merged range
+  b.n_sink = 0;
+  b.sink_first = 0;
+  if (s > 0 && lo >= s) {          // sinks lie left of every row's window
+    if (p.merge)
+      b.sink_first = 1;
+    else
+      b.n_sink = p.n_sink;
+  } else if (s > 0) {
+    lo = 0;                        // window reaches the sinks: one merged range
   }
   b.lo = lo;
   b.n_tiles = b.n_sink + cdiv_band(p, b.t_last - lo + 1);
@@ -154,38 +178,83 @@ struct ItemWalker {
   }
 };
 
+// One key tile. Its ncols columns are, in order: n_sink_cols columns holding
+// the sink box keys sink_key0, sink_key0 + 1, ... (loaded with the sink tensor
+// map), then the band columns holding keys k0, k0 + 1, ... of which the tile
+// owns [own_lo, own_hi) (no key is owned by two tiles of a block).
 struct Tile {
-  int k0;        // first key row loaded
-  int own_lo;    // keys this tile is responsible for: [own_lo, own_hi)
+  int n_sink_cols;
+  int sink_key0;
+  int k0;
+  int own_lo;
   int own_hi;
-  int ncols;     // MMA N: keys multiplied (multiple of 16, <= box rows)
-  bool sink;     // loaded with the sink tensor map (box of s_box rows)
+  int ncols;     // MMA N (multiple of 16, <= kMaxTileKeys)
   bool full;     // every (row, key) pair of the tile is admitted: no mask needed
 };
 
 SWA_HD Tile tile_at(const PrefillPlan &p, const BlockTiles &b, int i, int w, int s) {
   Tile t;
-  if (i < b.n_sink) {
-    t.sink = true;
-    t.own_lo = i * p.s_box;
-    t.own_hi = imin(s, t.own_lo + p.s_box);
-    t.k0 = t.own_lo;
+  if (i < b.n_sink) {            // a tile of one sink box
+    t.n_sink_cols = p.s_box;
+    t.sink_key0 = i * p.s_box;
+    t.k0 = 0;
+    t.own_lo = t.own_hi = 0;     // no band keys
     t.ncols = p.s_box;
-  } else {
-    t.sink = false;
-    t.k0 = b.lo + (i - b.n_sink) * p.n_band;
-    t.own_lo = t.k0;
-    t.own_hi = imin(t.k0 + p.n_band, b.t_last + 1);
-    t.ncols = imin(p.n_band, round_up(t.own_hi - t.own_lo, 16));
+    t.full = false;
+    return t;
   }
-  // Mask-free when all ncols keys are owned and, for every row t of the block
-  // (t0 .. t0+Tq-1), inside [t - w + 1, t]: the in-band interior tiles.
-  int t_hi = b.t0 + p.Tq - 1;
-  bool owned_all = (t.own_hi - t.own_lo) == t.ncols;
-  bool causal_ok = t.k0 + t.ncols - 1 <= b.t0;
-  bool window_ok = t.k0 >= t_hi - w + 1;
-  t.full = owned_all && causal_ok && window_ok && !t.sink;
+  const int bi = i - b.n_sink;
+  t.n_sink_cols = (b.sink_first && bi == 0) ? p.s_box : 0;
+  t.sink_key0 = 0;
+  t.k0 = b.lo + bi * p.n_band;
+  t.own_lo = t.k0;
+  t.own_hi = imin(t.k0 + p.n_band, b.t_last + 1);
+  // the loaded band box is n_band keys; columns past the owned keys are masked
+  t.ncols = imin(t.n_sink_cols + p.n_band, round_up(t.n_sink_cols + t.own_hi - t.own_lo, 32));
+  // Mask-free when all columns are owned band keys and, for every row t of the
+  // block (t0 .. t0+Tq-1), inside [t - w + 1, t]: the in-band interior tiles.
+  const int t_hi = b.t0 + p.Tq - 1;
+  const bool owned_all = t.n_sink_cols == 0 && (t.own_hi - t.own_lo) == t.ncols;
+  const bool causal_ok = t.k0 + t.ncols - 1 <= b.t0;
+  const bool window_ok = t.k0 >= t_hi - w + 1;
+  t.full = owned_all && causal_ok && window_ok;
   return t;
+}
+
+// The key held by column c of a tile.
+SWA_HD int tile_key(const Tile &t, int c) {
+  return c < t.n_sink_cols ? t.sink_key0 + c : t.k0 + (c - t.n_sink_cols);
+}
+
+// Whether query t admits column c of a tile (the tile's share of K(t)).
+SWA_HD bool tile_admit(const Tile &t, int c, int q, int w, int s) {
+  if (t.full) return true;
+  const int j = tile_key(t, c);
+  if (c < t.n_sink_cols) return j < s && j <= q;
+  return admit(q, j, w, s, t.own_lo, t.own_hi);
+}
+
+// The admitted columns of a tile for query t form at most two ranges of
+// column indices, [a_lo, a_hi) (band keys inside the window) and [b_lo, b_hi)
+// (sink keys); either may be empty.
+struct ColRanges {
+  int a_lo, a_hi, b_lo, b_hi;
+};
+
+SWA_HD ColRanges tile_ranges(const Tile &t, int q, int w, int s) {
+  ColRanges r;
+  const int off = t.n_sink_cols - t.k0;  // column of band key j is j + off
+  r.a_lo = imax(t.own_lo, q - w + 1) + off;
+  r.a_hi = imin(t.own_hi, q + 1) + off;
+  if (t.n_sink_cols > 0) {
+    r.b_lo = 0;
+    r.b_hi = imax(0, imin(imin(s, q + 1) - t.sink_key0, t.n_sink_cols));
+  } else {
+    // band keys below s are sinks too (the window reaches the sinks)
+    r.b_lo = t.own_lo + off;
+    r.b_hi = imin(imin(t.own_hi, s), q + 1) + off;
+  }
+  return r;
 }
 
 }  // namespace swa
