@@ -6,7 +6,7 @@ One step = one pass of the whole hot path over one batch of the Llama-3.1-8B
 shaped single-layer workload (B=1, L=4096, Hq=32, Hkv=8, d=128, SWA(w=128,
 s=4), bf16, q/k/v ~ N(0,1) with the four sink keys scaled x4):
     swa_prefill  ->  swa_cache_append (prompt survivors)
-                 ->  swa_cache_append (one new token)  ->  swa_decode (pos = L)
+                 ->  swa_append_decode (append one new token, decode at pos = L)
 Metric: in-band TFLOP/s = 4 * B * Hq * d * (sum over the step's query rows of
 |K(t)|) / step time. The decode half of the metric (KV GB/s at batch 64, 68-slot
 cache, SWA(64, 4)) is measured in the same run and reported under "decode".
@@ -205,10 +205,9 @@ class GpuStep:
         c = self.cfg
         self.swa.swa_cache_append(self.dev["k"], self.dev["v"], self.kc, self.vc, self.pos0,
                                   c["w"], c["s"])
-        self.swa.swa_cache_append(self.dev["kn"], self.dev["vn"], self.kc, self.vc, self.posL,
-                                  c["w"], c["s"])
-        self.swa.swa_decode(self.dev["qn"], self.kc, self.vc, self.posL, c["w"], c["s"],
-                            out=self.dec, workspace=self.ws)
+        self.swa.swa_append_decode(self.dev["qn"], self.dev["kn"][:, 0], self.dev["vn"][:, 0],
+                                   self.kc, self.vc, self.posL, c["w"], c["s"], out=self.dec,
+                                   workspace=self.ws)
 
     def capture(self, stream):
         self.graph_prefill = torch.cuda.CUDAGraph()
@@ -220,9 +219,10 @@ class GpuStep:
 
 
 def launches_per_step(swa, cfg) -> int:
+    """prefill + append(prompt) + append_decode (+ the split-KV combine)."""
     splits_ws = swa.swa_decode_workspace_size(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["w"],
                                               cfg["s"])
-    return 1 + 2 + (2 if splits_ws else 1)
+    return 1 + 1 + (2 if splits_ws else 1)
 
 
 def bench_decode(swa, device, stream, iters=64, warmup=8):
@@ -353,7 +353,7 @@ def run_gpu(args):
                        "Hkv": cfg["Hkv"], "d": cfg["d"], "w": cfg["w"], "s": cfg["s"],
                        "global_batch": cfg["B"] * world, "seq_len": cfg["L"],
                        "parallelism": f"replicas x{world}",
-                       "step": "prefill + append(prompt) + append(1) + decode(pos=L)",
+                       "step": "prefill + append(prompt) + append_decode(pos=L)",
                        "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
                              f"(> 126 MB L2), CUDA graph per set"},
             "roofline": roofline,

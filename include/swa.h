@@ -99,6 +99,18 @@ SWA_API int swa_decode(const void *q, const void *kcache, const void *vcache, co
                void *out, int B, int Hq, int Hkv, int d, int w, int s, float scale,
                void *workspace, size_t workspace_bytes, swa_stream_t stream);
 
+/* Append one new token per sequence, then decode it, in one launch: the same
+ * result (and cache contents) as swa_cache_append with T = 1 at pos[b]
+ * followed by swa_decode at pos[b] (the per-token step of the rolling cache,
+ * wiblog.cn long-context SWA article, section "与 KV Cache 的配合：轮转替换策略").
+ *   k_new, v_new [B, Hkv, d] bf16: the new token's key and value rows
+ *   pos DEVICE int32[B]: the new token's position (the cache holds every
+ *   earlier position); other arguments as swa_decode, same workspace size. */
+SWA_API int swa_append_decode(const void *q, const void *k_new, const void *v_new, void *kcache,
+                              void *vcache, const int *pos, void *out, int B, int Hq, int Hkv,
+                              int d, int w, int s, float scale, void *workspace,
+                              size_t workspace_bytes, swa_stream_t stream);
+
 /* Maximum scratch bytes swa_decode_noalloc can use (see below). */
 #define SWA_DECODE_NOALLOC_SCRATCH_BYTES (2u << 20)
 

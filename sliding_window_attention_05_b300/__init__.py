@@ -48,6 +48,9 @@ _lib.swa_decode_workspace_size.restype = _sz
 _lib.swa_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
 _lib.swa_decode.restype = _i
 _lib.swa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+_lib.swa_append_decode.restype = _i
+_lib.swa_append_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
+                                   _vp, _sz, _vp]
 _lib.swa_decode_noalloc.restype = _i
 _lib.swa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.swa_cache_slot.restype = ctypes.c_longlong
@@ -210,8 +213,37 @@ def swa_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, pos:
     return out
 
 
+def swa_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      kcache: torch.Tensor, vcache: torch.Tensor, pos: torch.Tensor, w: int, s: int,
+                      scale: float | None = None, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """Append the token k_new/v_new [B,Hkv,d] at position pos[b], then decode
+    q [B,Hq,d] over the cache (one launch)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
+                 (vcache, "vcache")):
+        _bf16_cuda(t, n)
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError("pos must be a CUDA int32 tensor")
+    B, Hq, d = q.shape
+    Hkv = kcache.shape[1]
+    if k_new.shape != (B, Hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new/v_new must be [B, Hkv, d] = {(B, Hkv, d)}")
+    if out is None:
+        out = torch.empty_like(q)
+    need = swa_decode_workspace_size(B, Hq, Hkv, d, w, s)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.swa_append_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                                  _ptr(pos), _ptr(out), B, Hq, Hkv, d, int(w), int(s),
+                                  _default_scale(d, scale), _ptr(workspace), wbytes,
+                                  _stream(stream)), "swa_append_decode")
+    return out
+
+
 cache_append = swa_cache_append
 decode = swa_decode
+append_decode = swa_append_decode
 
 
 class RingCache:
@@ -233,6 +265,20 @@ class RingCache:
         swa_cache_append(k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s, stream)
         self._last_pos.copy_(self.next_pos + (T - 1))
         self.next_pos.add_(T)
+
+    def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+             scale: float | None = None, out=None, stream=None):
+        """Append one token per sequence (k_new/v_new [B, Hkv, d]) and decode
+        q [B, Hq, d] at its position, in one launch."""
+        B, Hq, d = q.shape
+        need = swa_decode_workspace_size(B, Hq, self.Hkv, d, self.w, self.s)
+        if need and (self._workspace is None or self._workspace.numel() < need):
+            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        self._last_pos.copy_(self.next_pos)
+        res = swa_append_decode(q, k_new, v_new, self.k, self.v, self._last_pos, self.w, self.s,
+                                scale, out, self._workspace if need else None, stream)
+        self.next_pos.add_(1)
+        return res
 
     def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):
         """Attend q [B, Hq, d] (the newest token's queries) over the cache."""

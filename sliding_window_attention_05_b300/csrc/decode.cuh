@@ -9,10 +9,11 @@
 //
 // Decode is bandwidth-bound (about 4 flop per byte of cache read): it runs on
 // the CUDA cores. One CTA (4 warps) serves one (sequence, KV head, head group,
-// split): the G query heads sharing the KV head are packed so every K/V row is
-// read from memory once for all of them. Each key row (d bf16) is spread over
-// d/8 lanes that each load 16 bytes, so a warp-wide load covers 256 or 512
-// contiguous bytes; dot products are reduced with xor-shuffles.
+// split): the query heads sharing the KV head are packed, so every K/V row is
+// read from memory once for all of them. A CTA stages its whole slot range of
+// K and V (one contiguous run of each, at most kDecodeMaxKeys rows) into
+// shared memory with two bulk asynchronous copies issued at its start, so all
+// of its bytes are in flight at once; it then computes from shared memory.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -25,29 +26,35 @@ namespace swa {
 
 // ---------------------------------------------------------------- append
 
-// One thread moves 16 bytes of K and 16 bytes of V of one (b, token, kvh).
+// Only the tokens that survive the call are visited: token i (position
+// p0 + i) survives iff p0 + i < s (a sink) or i >= T - w (among the last w).
+// Survivor k of sequence b is token k if k < h, else token max(h, T - w) + k - h,
+// where h = clamp(s - p0, 0, T); there are at most min(T, s + w) of them.
+// One thread moves 16 bytes of K and 16 bytes of V of one (b, survivor, kvh).
 __global__ void swa_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                                   uint4 *__restrict__ kcache, uint4 *__restrict__ vcache,
                                   const int *__restrict__ pos_start, int T, int Hkv, int d, int w,
-                                  int s) {
+                                  int s, int max_survivors) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int b = blockIdx.y;
   const int vec_per_row = d / 8;
-  const long long n = (long long)T * Hkv * vec_per_row;
+  const long long n = (long long)max_survivors * Hkv * vec_per_row;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n) return;
   const int c = (int)(idx % vec_per_row);
   const int kvh = (int)((idx / vec_per_row) % Hkv);
-  const int i = (int)(idx / ((long long)vec_per_row * Hkv));
+  const int k = (int)(idx / ((long long)vec_per_row * Hkv));
   const int p0 = pos_start[b];
   if (p0 < 0) {
     if (idx == 0) record_error(kErrNegativePosition);
     return;
   }
+  const int h = imin(imax(s - p0, 0), T);       // survivors at the front (sinks)
+  const int tail0 = imax(h, T - w);             // first survivor of the tail
+  const int i = k < h ? k : tail0 + (k - h);    // token index
+  if (i >= T) return;
   const long long p = (long long)p0 + i;
-  const long long p_last = (long long)p0 + T - 1;
-  // A token that a later token of this call overwrites again is skipped.
-  const bool survives = p < s || p >= p_last - w + 1;
-  if (!survives) return;
   const long long slot = ring_slot(p, w, s);
   const long long src = (((long long)b * T + i) * Hkv + kvh) * vec_per_row + c;
   const long long dst = (((long long)b * Hkv + kvh) * (s + w) + slot) * vec_per_row + c;
@@ -57,15 +64,9 @@ __global__ void swa_append_kernel(const uint4 *__restrict__ k_new, const uint4 *
 
 // ---------------------------------------------------------------- decode
 
-constexpr int kDecodeWarps = 4;
-
-__device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
+constexpr int kDecodeThreads = 128;
+constexpr int kDecodeMaxKeys = 256;   // slots one CTA stages (128 KB of K+V at d = 128)
+constexpr int kDecodeMaxHeads = 4;    // query heads one CTA packs
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -76,27 +77,90 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8]) {
   }
 }
 
+// Bulk asynchronous copy global -> shared of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 struct DecodeArgs {
   const __nv_bfloat16 *q;
   const __nv_bfloat16 *kc;
   const __nv_bfloat16 *vc;
+  const __nv_bfloat16 *k_new;  // [B, Hkv, D] token appended at pos[b] first (or null)
+  const __nv_bfloat16 *v_new;
+  __nv_bfloat16 *kc_w;         // the caches, writable (used with k_new)
+  __nv_bfloat16 *vc_w;
   const int *pos;
   __nv_bfloat16 *out;
   float *part_o;     // [B, Hq, splits, D] when splits > 1
   float2 *part_ml;   // [B, Hq, splits] (running max in log2 units, sum)
   int Hq, Hkv, w, s, splits;
+  int max_keys;      // slots one CTA stages at most (sizes its shared memory)
   float scale_log2;
 };
 
-// HG query heads per CTA (a divisor of G); D = head dimension.
-// Key chunks of KPW * U keys are processed per warp iteration, double-buffered.
+constexpr int kDecodeChunk = kDecodeMaxKeys;  // keys per chunk: one chunk per CTA
+constexpr int kDecodeMaxChunks = kDecodeMaxKeys / kDecodeChunk;
+
+// Dynamic shared memory of one decode CTA.
 template <int D, int HG>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-    swa_decode_kernel(const DecodeArgs a) {
-  constexpr int LPK = D / 8;          // lanes per key row (16 bytes each)
-  constexpr int KPW = 32 / LPK;       // keys per warp-wide load
-  constexpr int U = HG >= 4 ? 2 : 4;  // loads per lane per chunk
-  constexpr int CH = KPW * U;         // keys per chunk
+struct DecodeSmem {
+  static size_t bytes(int max_keys) {
+    return 128 /* alignment */ + 256 /* barriers */ + 2 * (size_t)max_keys * D * 2 +
+           2 * (size_t)(max_keys < kDecodeChunk ? max_keys : kDecodeChunk) * HG * 4 /* P */ +
+           3 * HG * 4 + 16 +
+           (size_t)kDecodeThreads * HG * 8;
+  }
+};
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t *>(&a)), "l"(*reinterpret_cast<uint64_t *>(&b)),
+        "l"(*reinterpret_cast<uint64_t *>(&c)));
+  return *reinterpret_cast<float2 *>(&r);
+}
+
+// two bf16 (low half first) -> two floats
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// HG query heads per CTA (a divisor of G, at most 4); D = head dimension.
+//
+// The CTA's slots are consumed in chunks of kDecodeChunk keys (the K and V of
+// every chunk requested at once, one bulk copy each with its own barrier) with
+// an online softmax across chunks; with kDecodeChunk = kDecodeMaxKeys a CTA
+// has a single chunk, K first and V second, so the scores start while V is
+// still arriving.
+template <int D, int HG>
+__global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const DecodeArgs a) {
+  constexpr int LPK = 8;            // lanes per key row in the score phase
+  constexpr int EPL = D / LPK;      // elements of a row per lane (16 or 8)
+  constexpr int kPairs = D / 2;     // column pairs of a row
+  constexpr int kParts = kDecodeThreads / kPairs;  // key parts in the P V phase
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) &
+                                             ~uintptr_t(127));
+  uint64_t *bar_k = reinterpret_cast<uint64_t *>(dsm);                  // [kDecodeMaxChunks]
+  uint64_t *bar_v = bar_k + kDecodeMaxChunks;                           // [kDecodeMaxChunks]
+  __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(dsm + 256);     // [max_keys][D]
+  __nv_bfloat16 *sV = sK + (size_t)a.max_keys * D;                       // [max_keys][D]
+  const int pchunk = imin(kDecodeChunk, a.max_keys);                  // keys of a P buffer
+  float *sP = reinterpret_cast<float *>(sV + (size_t)a.max_keys * D);  // [2][pchunk][HG]
+  float *sM = sP + 2 * pchunk * HG;                                    // [HG] running max
+  float *sL = sM + HG;                                                 // [HG] running sum
+  float *sF = sL + HG;                                                 // [HG] rescale factor
+  float2 *sO = reinterpret_cast<float2 *>(                             // [kParts][HG][kPairs]
+      (reinterpret_cast<uintptr_t>(sF + HG) + 15) & ~uintptr_t(15));
+  __shared__ int abort_word;
 
   const int split = blockIdx.x;
   const int G = a.Hq / a.Hkv;
@@ -105,9 +169,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int hg = blockIdx.y % hgroups;
   const int b = blockIdx.z;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kg = lane / LPK;          // which key of a warp-wide load
-  const int dl = lane % LPK;          // which 8-element slice of d
+  const int hq0 = kvh * G + hg * HG;
 
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int pos = a.pos[b];
   if (pos < 0) {
     if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) record_error(kErrNegativePosition);
@@ -116,165 +181,207 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int n = ring_valid(pos, a.w, a.s);
   const int per_split = cdiv(n, a.splits);
   const int k_begin = imin(n, split * per_split);
-  const int k_end = imin(n, k_begin + per_split);
-
-  // queries of the HG heads, this lane's slice, pre-scaled to log2 units
-  float qf[HG][8];
-  const int hq0 = kvh * G + hg * HG;
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    const uint4 raw = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.Hq + hq0 + h) * D + dl * 8);
-    bf16x8_to_f32(raw, qf[h]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qf[h][e] *= a.scale_log2;
-  }
-
-  const size_t row_base = ((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w);
-  const uint4 *kc = reinterpret_cast<const uint4 *>(a.kc + row_base * D) + dl;
-  const uint4 *vc = reinterpret_cast<const uint4 *>(a.vc + row_base * D) + dl;
-
-  float m[HG], l[HG], o[HG][8];
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
-  }
-
-  // chunks of this split are dealt round-robin to the warps; two register
-  // buffers alternate (static indices) so the next chunk's loads are in flight
-  // while the current one is reduced
-  const int n_chunks = cdiv(k_end - k_begin, CH);
-  uint4 ka[U], va[U], kb[U], vb[U];
-  auto load_chunk = [&](int ci, uint4 (&kr)[U], uint4 (&vr)[U]) {
-    const int base = k_begin + ci * CH;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int key = base + u * KPW + kg;
-      if (key < k_end) {
-        kr[u] = ld_stream_v4(kc + (size_t)key * LPK);
-        vr[u] = ld_stream_v4(vc + (size_t)key * LPK);
-      } else {
-        kr[u] = make_uint4(0, 0, 0, 0);
-        vr[u] = make_uint4(0, 0, 0, 0);
+  const int nk = imin(n, k_begin + per_split) - k_begin;  // <= max_keys
+  const int n_chunks = cdiv(nk, kDecodeChunk);
+  // With k_new: the token at position pos goes to ring slot(pos). Every CTA
+  // that stages that slot patches its shared-memory copy; the first head
+  // group's CTA also writes it to the cache.
+  int append_row = -1;
+  if (a.k_new != nullptr) {
+    const int slot = (int)ring_slot(pos, a.w, a.s);
+    if (slot >= k_begin && slot < k_begin + nk) {
+      append_row = slot - k_begin;
+      if (hg == 0 && threadIdx.x < D / 4) {
+        const size_t src = ((size_t)b * a.Hkv + kvh) * D;
+        const size_t dst = (((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w) + slot) * D;
+        const int u = threadIdx.x % (D / 8);
+        if (threadIdx.x < D / 8)
+          reinterpret_cast<uint4 *>(a.kc_w + dst)[u] = reinterpret_cast<const uint4 *>(a.k_new + src)[u];
+        else
+          reinterpret_cast<uint4 *>(a.vc_w + dst)[u] = reinterpret_cast<const uint4 *>(a.v_new + src)[u];
       }
     }
-  };
-  auto consume = [&](int ci, const uint4 (&kr)[U], const uint4 (&vr)[U]) {
-    const int base = k_begin + ci * CH;
-    float sc[HG][U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float kf[8];
-      bf16x8_to_f32(kr[u], kf);
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-        sc[h][u] = acc;
-      }
-    }
-    // sum the partial dots over the LPK lanes of each key
-#pragma unroll
-    for (int off = LPK / 2; off >= 1; off /= 2)
-#pragma unroll
-      for (int h = 0; h < HG; ++h)
-#pragma unroll
-        for (int u = 0; u < U; ++u) sc[h][u] += __shfl_xor_sync(0xffffffffu, sc[h][u], off);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool valid = base + u * KPW + kg < k_end;
-#pragma unroll
-      for (int h = 0; h < HG; ++h)
-        if (!valid) sc[h][u] = -INFINITY;
-    }
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      float cm = sc[h][0];
-#pragma unroll
-      for (int u = 1; u < U; ++u) cm = fmaxf(cm, sc[h][u]);
-#pragma unroll
-      for (int off = LPK; off < 32; off *= 2) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-      const float m_new = fmaxf(m[h], cm);  // finite: every chunk holds a valid key
-      const float f = fast_exp2(m[h] - m_new);
-      m[h] = m_new;
-      l[h] *= f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] *= f;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float p = fast_exp2(sc[h][u] - m_new);
-        l[h] += p;
-        float vf[8];
-        bf16x8_to_f32(vr[u], vf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(p, vf[e], o[h][e]);
-      }
-    }
-  };
-
-  constexpr int W = kDecodeWarps;
-  if (warp < n_chunks) load_chunk(warp, ka, va);
-  for (int ci = warp; ci < n_chunks; ci += 2 * W) {
-    if (ci + W < n_chunks) load_chunk(ci + W, kb, vb);
-    consume(ci, ka, va);
-    if (ci + W >= n_chunks) break;
-    if (ci + 2 * W < n_chunks) load_chunk(ci + 2 * W, ka, va);
-    consume(ci + W, kb, vb);
   }
 
-  // combine the KPW key groups of the warp (same d slice, different keys)
+  const size_t row_base = ((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w) + k_begin;
+  if (threadIdx.x == 0) {
+    abort_word = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      mbar_init(&bar_k[c], 1);
+      mbar_init(&bar_v[c], 1);
+    }
+    fence_mbar_init();
+    // every chunk's K first, then every chunk's V: the scores need K first
+    for (int c = 0; c < n_chunks; ++c) {
+      const int kc = imin(kDecodeChunk, nk - c * kDecodeChunk);
+      const uint32_t bytes = (uint32_t)kc * D * 2;
+      mbar_arrive_expect_tx(&bar_k[c], bytes);
+      bulk_load(sK + (size_t)c * kDecodeChunk * D, a.kc + (row_base + c * kDecodeChunk) * D,
+                bytes, &bar_k[c]);
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+      const int kc = imin(kDecodeChunk, nk - c * kDecodeChunk);
+      const uint32_t bytes = (uint32_t)kc * D * 2;
+      mbar_arrive_expect_tx(&bar_v[c], bytes);
+      bulk_load(sV + (size_t)c * kDecodeChunk * D, a.vc + (row_base + c * kDecodeChunk) * D,
+                bytes, &bar_v[c]);
+    }
+  }
+  if (threadIdx.x < HG) {
+    sM[threadIdx.x] = -INFINITY;
+    sL[threadIdx.x] = 0.f;
+  }
+  // queries of the HG heads, this lane's slice as pairs, pre-scaled to log2 units
+  const int kg = lane / LPK;   // which of the 4 keys of a warp step
+  const int dl = lane % LPK;   // which slice of d
+  float2 q2[HG][EPL / 2];
 #pragma unroll
   for (int h = 0; h < HG; ++h) {
 #pragma unroll
-    for (int off = LPK; off < 32; off *= 2) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+    for (int v = 0; v < EPL / 8; ++v) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.Hq + hq0 + h) * D +
+                                                         dl * EPL + v * 8);
+      const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = bf16x2_to_f2(wd[e]);
+        q2[h][v * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+      }
     }
   }
+  const int cp = threadIdx.x % kPairs, part = threadIdx.x / kPairs;  // P V phase mapping
+  float2 o2[HG];
+#pragma unroll
+  for (int h = 0; h < HG; ++h) o2[h] = make_float2(0.f, 0.f);
+  __syncthreads();  // barriers initialised
 
-  // combine the warps through shared memory
-  __shared__ float sm_m[kDecodeWarps][HG], sm_l[kDecodeWarps][HG];
-  __shared__ float sm_o[kDecodeWarps][HG][D];
-  if (lane < LPK) {
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm_o[warp][h][dl * 8 + e] = o[h][e];
+  for (int c = 0; c < n_chunks; ++c) {
+    const int j_base = c * kDecodeChunk;
+    const int kc = imin(kDecodeChunk, nk - j_base);
+    float *sPc = sP + (c & 1) * pchunk * HG;  // [pchunk][HG]
+    // one thread polls the barrier; the others sleep in __syncthreads
+    if (threadIdx.x == 0) mbar_wait(&bar_k[c], 0, &abort_word);
+    __syncthreads();
+    if (append_row >= j_base && append_row < j_base + kc) {
+      // the appended token's slot: its staged row still holds the old entry
+      if (threadIdx.x < D / 8)
+        reinterpret_cast<uint4 *>(sK + (size_t)append_row * D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(a.k_new + ((size_t)b * a.Hkv + kvh) * D)[threadIdx.x];
+      __syncthreads();
     }
-  }
-  if (lane == 0) {
+    // ---- scores of the chunk: each warp step covers 4 keys, 8 lanes per key
+    for (int j0 = warp * 4; j0 < kc; j0 += 4 * (kDecodeThreads / 32)) {
+      const int j = j0 + kg;
+      float2 acc2[HG];
 #pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      sm_m[warp][h] = m[h];
-      sm_l[warp][h] = l[h];
+      for (int h = 0; h < HG; ++h) acc2[h] = make_float2(0.f, 0.f);
+      if (j < kc) {
+#pragma unroll
+        for (int v = 0; v < EPL / 8; ++v) {
+          const uint4 raw =
+              *reinterpret_cast<const uint4 *>(sK + (size_t)(j_base + j) * D + dl * EPL + v * 8);
+          const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kf = bf16x2_to_f2(wd[e]);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) acc2[h] = ffma2(q2[h][v * 4 + e], kf, acc2[h]);
+          }
+        }
+      }
+      float acc[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) acc[h] = acc2[h].x + acc2[h].y;
+#pragma unroll
+      for (int off = LPK / 2; off >= 1; off /= 2)
+#pragma unroll
+        for (int h = 0; h < HG; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
+      if (dl == 0 && j < kc) {
+#pragma unroll
+        for (int h = 0; h < HG; ++h) sPc[j * HG + h] = acc[h];
+      }
     }
+    __syncthreads();
+    // ---- online softmax update of each head (warp h)
+    if (warp < HG) {
+      float mc = -INFINITY;
+      for (int j = lane; j < kc; j += 32) mc = fmaxf(mc, sPc[j * HG + warp]);
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+      const float m_old = sM[warp];
+      const float m_new = fmaxf(m_old, mc);
+      float ls = 0.f;
+      for (int j = lane; j < kc; j += 32) {
+        const float p = fast_exp2(sPc[j * HG + warp] - m_new);
+        sPc[j * HG + warp] = p;
+        ls += p;
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      if (lane == 0) {
+        const float f = m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new);
+        sF[warp] = f;
+        sM[warp] = m_new;
+        sL[warp] = sL[warp] * f + ls;
+      }
+    }
+    if (threadIdx.x == 0) mbar_wait(&bar_v[c], 0, &abort_word);
+    __syncthreads();
+    if (append_row >= j_base && append_row < j_base + kc) {
+      if (threadIdx.x < D / 8)
+        reinterpret_cast<uint4 *>(sV + (size_t)append_row * D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(a.v_new + ((size_t)b * a.Hkv + kvh) * D)[threadIdx.x];
+      __syncthreads();
+    }
+    // ---- O = O * f + P V over the chunk: thread = (column pair, key part);
+    // one V pair feeds all HG heads (consecutive threads: consecutive pairs)
+    {
+      float f[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) f[h] = sF[h];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) o2[h] = make_float2(o2[h].x * f[h], o2[h].y * f[h]);
+      const int per_part = cdiv(kc, kParts);
+      const int j_lo = imin(kc, part * per_part), j_hi = imin(kc, j_lo + per_part);
+      const uint32_t *vcol = reinterpret_cast<const uint32_t *>(sV + (size_t)j_base * D) + cp;
+      for (int j = j_lo; j < j_hi; ++j) {
+        const float2 vf = bf16x2_to_f2(vcol[(size_t)j * kPairs]);
+        float pr[HG];
+        if constexpr (HG == 4) {
+          const float4 p4 = *reinterpret_cast<const float4 *>(sPc + j * 4);
+          pr[0] = p4.x; pr[1] = p4.y; pr[2] = p4.z; pr[3] = p4.w;
+        } else {
+#pragma unroll
+          for (int h = 0; h < HG; ++h) pr[h] = sPc[j * HG + h];
+        }
+#pragma unroll
+        for (int h = 0; h < HG; ++h) o2[h] = ffma2(make_float2(pr[h], pr[h]), vf, o2[h]);
+      }
+    }
+    // the next chunk writes the other P buffer; the one after that reuses
+    // this one only after the next chunk's barrier
   }
+#pragma unroll
+  for (int h = 0; h < HG; ++h) sO[(part * HG + h) * kPairs + cp] = o2[h];
   __syncthreads();
-  for (int idx = threadIdx.x; idx < HG * D; idx += blockDim.x) {
-    const int h = idx / D, e = idx % D;
-    float M = -INFINITY;
+  for (int item = threadIdx.x; item < HG * kPairs; item += kDecodeThreads) {
+    const int h = item / kPairs, cq = item % kPairs;
+    float2 o = sO[h * kPairs + cq];
 #pragma unroll
-    for (int wi = 0; wi < kDecodeWarps; ++wi) M = fmaxf(M, sm_m[wi][h]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int wi = 0; wi < kDecodeWarps; ++wi) {
-        const float f = fast_exp2(sm_m[wi][h] - M);  // 0 for warps without keys
-        num += f * sm_o[wi][h][e];
-        den += f * sm_l[wi][h];
-      }
+    for (int pp = 1; pp < kParts; ++pp) {
+      const float2 x = sO[(pp * HG + h) * kPairs + cq];
+      o.x += x.x;
+      o.y += x.y;
     }
     const int hq = hq0 + h;
     if (a.splits == 1) {
-      a.out[((size_t)b * a.Hq + hq) * D + e] = __float2bfloat16_rn(num / den);
+      const float inv = 1.0f / sL[h];
+      reinterpret_cast<uint32_t *>(a.out + ((size_t)b * a.Hq + hq) * D)[cq] =
+          pack_bf16x2(o.x * inv, o.y * inv);
     } else {
       const size_t pi = ((size_t)b * a.Hq + hq) * a.splits + split;
-      a.part_o[pi * D + e] = num;
-      if (e == 0) a.part_ml[pi] = make_float2(M, den);
+      reinterpret_cast<float2 *>(a.part_o + pi * D)[cq] = o;
+      if (cq == 0) a.part_ml[pi] = nk > 0 ? make_float2(sM[h], sL[h]) : make_float2(-INFINITY, 0.f);
     }
   }
 }
@@ -285,6 +392,8 @@ __global__ void __launch_bounds__(D) swa_decode_combine_kernel(const float *__re
                                                                const float2 *__restrict__ part_ml,
                                                                __nv_bfloat16 *__restrict__ out,
                                                                int splits) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const size_t bh = blockIdx.x;
   const int e = threadIdx.x;
   float M = -INFINITY;

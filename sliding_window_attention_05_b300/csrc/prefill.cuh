@@ -280,6 +280,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touched only this CTA's own resources; global memory is
+  // read and written only after the kernels this one depends on are done.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   const int BH = a.B * a.Hkv;
 

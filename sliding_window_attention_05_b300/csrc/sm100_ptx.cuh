@@ -33,6 +33,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic launch
+
+// Let the next kernel on the stream start launching (its CTAs run their
+// prologue while this grid finishes). Harmless without a dependent launch.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the kernels this one depends on have completed and their memory
+// is visible. A no-op when the kernel was not launched as a dependent.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

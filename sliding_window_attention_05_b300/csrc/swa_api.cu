@@ -71,6 +71,28 @@ int current_device_info(DeviceInfo *info) {
   return SWA_OK;
 }
 
+// ------------------------------------------------------------------ launches
+
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel on the stream finishes; it waits for that kernel
+// (griddepcontrol.wait) before touching global memory. In a captured CUDA
+// graph this becomes a programmatic edge.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------ tensor maps
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -173,34 +195,46 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.kv_chunk = swa::PrefillSmem<D>::chunk_bytes(plan);
   a.sep_stage = sep_stage ? 1 : 0;
   const int grid = swa::imin(a.n_items, dev.sms);
-  swa::swa_prefill_kernel<D><<<grid, swa::kPrefillThreads, smem, stream>>>(tq, tk, tv, tks, tvs, to,
-                                                                         a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(swa::swa_prefill_kernel<D>, dim3(grid), dim3(swa::kPrefillThreads),
+                             smem, stream, tq, tk, tv, tks, tvs, to, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "swa_prefill launch");
   return SWA_OK;
 }
 
 // ------------------------------------------------------------------ decode
 
-constexpr int kDecodeTargetCtas = 296;  // two waves' worth of CTAs on 148 SMs
-constexpr int kDecodeMinKeysPerSplit = 64;
-
-int head_group(int G) {
-  if (G % 8 == 0) return 8;
+// Query heads one decode CTA packs: the largest of 4, 2, 1 that divides G,
+// unless the (sequence, KV head) pairs are too few to fill the GPU; then one
+// head per CTA (the K/V rows shared by a group are read again from L2).
+int head_group(int B, int Hq, int Hkv) {
+  const int G = Hq / Hkv;
+  if ((long long)B * Hkv * 2 < 148) return 1;
   if (G % 4 == 0) return 4;
   if (G % 2 == 0) return 2;
   return 1;
 }
 
+// The cache of each (sequence, KV head) is split over CTAs when it holds
+// more slots than one CTA stages, or when there are too few (sequence, KV
+// head, head group) units to fill the GPU and the cache is long. The count is
+// fixed from the capacity s + w (positions are only known on the device).
 int decode_splits(int B, int Hq, int Hkv, int w, int s) {
   const int G = Hq / Hkv;
-  const long long units = (long long)B * Hkv * (G / head_group(G));
-  if (units >= kDecodeTargetCtas) return 1;
-  long long sp = (kDecodeTargetCtas + units - 1) / units;
-  const long long cap = ((long long)s + w + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
-  if (sp > cap) sp = cap;
-  if (sp < 1) sp = 1;
-  return (int)sp;
+  const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv));
+  const long long cap = (long long)s + w;
+  long long sp = (cap + swa::kDecodeMaxKeys - 1) / swa::kDecodeMaxKeys;
+  if (units < 148 && cap > 512) {
+    long long fill = (296 + units - 1) / units;
+    const long long most = (cap + 63) / 64;
+    if (fill > most) fill = most;
+    if (fill > sp) sp = fill;
+  }
+  return (int)(sp < 1 ? 1 : sp);
+}
+
+int decode_max_keys(int w, int s, int splits) {
+  return (int)(((long long)s + w + splits - 1) / splits);
 }
 
 size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
@@ -213,19 +247,26 @@ size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
 template <int D, int HG>
 cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
+  const size_t smem = swa::DecodeSmem<D, HG>::bytes(a.max_keys);
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(swa::swa_decode_kernel<D, HG>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)swa::DecodeSmem<D, HG>::bytes(swa::kDecodeMaxKeys));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(a.splits, a.Hkv * (G / HG), B);
-  swa::swa_decode_kernel<D, HG><<<grid, swa::kDecodeWarps * 32, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(swa::swa_decode_kernel<D, HG>, grid, dim3(swa::kDecodeThreads),
+                             smem, stream, a);
   if (e != cudaSuccess || a.splits == 1) return e;
-  swa::swa_decode_combine_kernel<D><<<B * a.Hq, D, 0, stream>>>(a.part_o, a.part_ml, a.out,
-                                                               a.splits);
-  return cudaGetLastError();
+  return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(B * a.Hq), dim3(D), 0, stream,
+                    a.part_o, a.part_ml, a.out, a.splits);
 }
 
 template <int D>
 cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
-  switch (head_group(a.Hq / a.Hkv)) {
-    case 8: return launch_decode_t<D, 8>(a, B, stream);
+  switch (head_group(B, a.Hq, a.Hkv)) {
     case 4: return launch_decode_t<D, 4>(a, B, stream);
     case 2: return launch_decode_t<D, 2>(a, B, stream);
     default: return launch_decode_t<D, 1>(a, B, stream);
@@ -363,16 +404,17 @@ int swa_cache_append(const void *k_new, const void *v_new, void *kcache, void *v
   DeviceInfo dev;
   int rc = current_device_info(&dev);
   if (rc) return rc;
-  const long long n = (long long)T * Hkv * (d / 8);
+  // only the tokens that survive the call are visited: at most s + w of them
+  const int max_surv = (int)(T < (long long)s + w ? T : (long long)s + w);
+  const long long n = (long long)max_surv * Hkv * (d / 8);
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
   if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "append too large");
-  swa::swa_append_kernel<<<dim3((unsigned)blocks, B), threads, 0,
-                           reinterpret_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
-      reinterpret_cast<uint4 *>(kcache), reinterpret_cast<uint4 *>(vcache), pos_start, T, Hkv, d,
-      w, s);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(
+      swa::swa_append_kernel, dim3((unsigned)blocks, B), dim3(threads), 0,
+      reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *>(k_new),
+      reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(kcache),
+      reinterpret_cast<uint4 *>(vcache), pos_start, T, Hkv, d, w, s, max_surv);
   if (e != cudaSuccess) return cuda_fail(e, "swa_cache_append launch");
   return SWA_OK;
 }
@@ -382,9 +424,33 @@ size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {
   return decode_workspace(B, Hq, Hkv, d, w, s);
 }
 
+int decode_impl(const void *q, const void *k_new, const void *v_new, const void *kcache,
+                const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
+                int w, int s, float scale, void *workspace, size_t workspace_bytes,
+                swa_stream_t stream);
+
 int swa_decode(const void *q, const void *kcache, const void *vcache, const int *pos, void *out,
                int B, int Hq, int Hkv, int d, int w, int s, float scale, void *workspace,
                size_t workspace_bytes, swa_stream_t stream) {
+  return decode_impl(q, nullptr, nullptr, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale,
+                     workspace, workspace_bytes, stream);
+}
+
+int swa_append_decode(const void *q, const void *k_new, const void *v_new, void *kcache,
+                      void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
+                      int w, int s, float scale, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream) {
+  if (!k_new || !v_new) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_new) || !aligned16(v_new))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  return decode_impl(q, k_new, v_new, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale,
+                     workspace, workspace_bytes, stream);
+}
+
+int decode_impl(const void *q, const void *k_new, const void *v_new, const void *kcache,
+                const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
+                int w, int s, float scale, void *workspace, size_t workspace_bytes,
+                swa_stream_t stream) {
   if (!q || !kcache || !vcache || !pos || !out) return fail(SWA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
     return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -405,6 +471,10 @@ int swa_decode(const void *q, const void *kcache, const void *vcache, const int 
   a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
   a.kc = reinterpret_cast<const __nv_bfloat16 *>(kcache);
   a.vc = reinterpret_cast<const __nv_bfloat16 *>(vcache);
+  a.k_new = reinterpret_cast<const __nv_bfloat16 *>(k_new);
+  a.v_new = reinterpret_cast<const __nv_bfloat16 *>(v_new);
+  a.kc_w = const_cast<__nv_bfloat16 *>(a.kc);
+  a.vc_w = const_cast<__nv_bfloat16 *>(a.vc);
   a.pos = pos;
   a.out = reinterpret_cast<__nv_bfloat16 *>(out);
   a.Hq = Hq;
@@ -412,6 +482,7 @@ int swa_decode(const void *q, const void *kcache, const void *vcache, const int 
   a.w = w;
   a.s = s;
   a.splits = decode_splits(B, Hq, Hkv, w, s);
+  a.max_keys = decode_max_keys(w, s, a.splits);
   a.scale_log2 = scale * 1.4426950408889634f;
   const size_t n = (size_t)B * Hq * a.splits;
   a.part_o = a.splits > 1 ? reinterpret_cast<float *>(workspace) : nullptr;

@@ -186,3 +186,45 @@ def test_hybrid_stack_prefill_then_decode():
             keys = oracle.keyset(pos, w, s)
             r, _ = oracle.decode(qs[i, 0], keys, hist_k[keys], hist_v[keys], pos, w, s, sc)
             compare(dec[i][0].cpu(), r, f"layer {layer} decode step {i}")
+
+
+@pytest.mark.parametrize("case", [
+    # B, L, Hq, Hkv, d, w, s
+    (1, 256, 4, 1, 64, 64, 4),
+    (2, 150, 32, 8, 128, 16, 4),
+    (1, 120, 6, 2, 64, 9, 0),
+    (2, 90, 16, 2, 64, 200, 4),
+], ids=lambda c: "B%d_L%d_Hq%d_Hkv%d_d%d_w%d_s%d" % c)
+def test_append_decode_equals_prefill_rows(case):
+    """swa_append_decode (append the token, then decode it, in one launch)
+    reproduces every prefill row, and leaves the cache bit-identical to
+    swa_cache_append."""
+    B, L, Hq, Hkv, d, w, s = case
+    q, k, v = prefill_case(B, L, Hq, Hkv, d, 4700 + L, sink_rows=min(s, L))
+    sc = scale_for(d)
+    ref, _ = oracle.prefill(q, k, v, w, s, sc)
+    fused = swa.RingCache(B, Hkv, d, w, s)
+    plain = swa.RingCache(B, Hkv, d, w, s)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    outs = []
+    for t in range(L):
+        outs.append(fused.step(qd[:, t].contiguous(), kd[:, t].contiguous(), vd[:, t].contiguous(), sc))
+        plain.append(kd[:, t:t + 1].contiguous(), vd[:, t:t + 1].contiguous())
+    dec = torch.stack(outs, dim=1)
+    torch.cuda.synchronize()
+    compare(dec.cpu(), ref, "append_decode")
+    assert torch.equal(_bits(fused.k), _bits(plain.k)) and torch.equal(_bits(fused.v), _bits(plain.v))
+
+
+@pytest.mark.parametrize("w,s,pos", [(2048, 100, 5000), (16640, 0, 9000)])
+def test_append_decode_split_kv(w, s, pos):
+    """The fused call on the split-KV path (one sequence, long cache)."""
+    B, Hq, Hkv, d = 1, 32, 8, 128
+    _, k, v = prefill_case(B, pos + 1, Hkv, Hkv, d, 4800 + pos)
+    q = swa_inputs.decode_query(B, Hq, d, 4900 + pos)
+    cache = swa.RingCache(B, Hkv, d, w, s)
+    cache.append(k[:, :pos].cuda(), v[:, :pos].cuda())
+    out = cache.step(q.cuda(), k[:, pos].contiguous().cuda(), v[:, pos].contiguous().cuda()).cpu()
+    keys = oracle.keyset(pos, w, s)
+    ref, _ = oracle.decode(q[0], keys, k[0, keys], v[0, keys], pos, w, s, scale_for(d))
+    compare(out[0], ref, f"fused split w={w} s={s} pos={pos}")
