@@ -305,47 +305,77 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int q_issued = 0;      // Q loads issued (one per item)
       int it = 0;
       bool ok = true;
-      for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
-           wk.next(), ++it) {
-        const int qb = wk.qb();
-        const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
-        const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
-        const int qbuf = it & 1;
-        // Order of loads: K of the first tile, Q, then the rest. That K's ring
-        // slot frees up when an earlier block's S is done, while the Q buffer
-        // may wait for an earlier block; Q must precede every V load, since a
-        // V slot frees up only after a P V that the MMA warp issues after the
-        // next S, which needs this Q.
-        for (int i = 0; i < bt.n_tiles; ++i) {
-          const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+      // The ring is filled in the order the MMA warp consumes it: K of tile g,
+      // then V of tile g - 1 (S_g is issued before P V_{g-1}, across blocks
+      // too), and the last V at the end. K_g then reuses the slot of a V that
+      // was consumed two tiles earlier, so its load is in flight long before
+      // S_g needs it. Q of a block follows the K of its first tile; every load
+      // before it is consumed by an MMA that does not need that Q.
+      Tile prev{};
+      int prev_b = 0, prev_kvh = 0;
+      bool have_prev = false, done = false;
+      ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb);
+      int i = 0, b = 0, kvh = 0;
+      BlockTiles bt{};
+      if (wk.valid()) {
+        b = wk.bh() / a.Hkv;
+        kvh = wk.bh() % a.Hkv;
+        bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      } else {
+        done = true;
+      }
+      while (ok && (!done || have_prev)) {
+        Tile tl{};
+        if (!done) tl = tile_at(plan, bt, i, a.w, a.s);
+        for (int half = 0; half < 2; ++half) {  // 0: K of this tile, 1: V of the previous one
+          if (half == 0 && done) continue;
+          if (half == 1 && !have_prev) continue;
+          const Tile &t = half == 0 ? tl : prev;
+          const int tb = half == 0 ? b : prev_b, th = half == 0 ? kvh : prev_kvh;
           // slot rows [0, n_sink_cols): the sink box; then the band box
-          const bool band = tl.ncols > tl.n_sink_cols;
+          const bool band = t.ncols > t.n_sink_cols;
           const uint32_t tile_bytes =
-              (uint32_t)(kChunks * 128 * (tl.n_sink_cols + (band ? plan.n_band : 0)));
-          for (int half = 0; half < 2; ++half) {  // 0: K, 1: V
-            if (i == 0 && half == 1) {
-              if (!mbar_wait(&q_empty[qbuf], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-              mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)(kChunks * 64 * plan.rows * 2));
-              for (int c = 0; c < kChunks; ++c)
-                tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
-                            kvh * plan.G, bt.t0, b, pol_q);
-              ++q_issued;
-            }
-            if (!mbar_wait(&kv_empty[slot], phase ^ 1, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(&kv_full[slot], tile_bytes);
-            uint8_t *dst = sKV + slot * slot_bytes;
-            for (int c = 0; c < kChunks; ++c) {
-              if (tl.n_sink_cols)
-                tma_load_4d(dst + c * kv_chunk, half == 0 ? &tm_ks : &tm_vs, &kv_full[slot],
-                            c * 64, kvh, tl.sink_key0, b, pol_kv);
-              if (band)
-                tma_load_4d(dst + c * kv_chunk + tl.n_sink_cols * 128, half == 0 ? &tm_k : &tm_v,
-                            &kv_full[slot], c * 64, kvh, tl.k0, b, pol_kv);
-            }
-            ++u;
-            if (++slot == stages) { slot = 0; phase ^= 1; }
+              (uint32_t)(kChunks * 128 * (t.n_sink_cols + (band ? plan.n_band : 0)));
+          if (!mbar_wait(&kv_empty[slot], phase ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&kv_full[slot], tile_bytes);
+          uint8_t *dst = sKV + slot * slot_bytes;
+          for (int c = 0; c < kChunks; ++c) {
+            if (t.n_sink_cols)
+              tma_load_4d(dst + c * kv_chunk, half == 0 ? &tm_ks : &tm_vs, &kv_full[slot],
+                          c * 64, th, t.sink_key0, tb, pol_kv);
+            if (band)
+              tma_load_4d(dst + c * kv_chunk + t.n_sink_cols * 128, half == 0 ? &tm_k : &tm_v,
+                          &kv_full[slot], c * 64, th, t.k0, tb, pol_kv);
           }
-          if (!ok) break;
+          ++u;
+          if (++slot == stages) { slot = 0; phase ^= 1; }
+          if (half == 0 && i == 0) {
+            const int qbuf = it & 1;
+            if (!mbar_wait(&q_empty[qbuf], ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)(kChunks * 64 * plan.rows * 2));
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
+                          kvh * plan.G, bt.t0, b, pol_q);
+            ++q_issued;
+          }
+        }
+        if (!ok) break;
+        have_prev = !done;
+        if (done) break;
+        prev = tl;
+        prev_b = b;
+        prev_kvh = kvh;
+        if (++i == bt.n_tiles) {
+          i = 0;
+          ++it;
+          wk.next();
+          if (wk.valid()) {
+            b = wk.bh() / a.Hkv;
+            kvh = wk.bh() % a.Hkv;
+            bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+          } else {
+            done = true;
+          }
         }
       }
       if (!ok) {
@@ -379,33 +409,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint64_t vd0 = sdesc_sw128(smem_u32(sKV), (uint32_t)kv_chunk, 1024);
     const uint32_t slot_step = (uint32_t)slot_bytes >> 4;
     const uint32_t kvc16 = (uint32_t)kv_chunk >> 4;
-    // K of tile g is load 2g, V of tile g is load 2g + 1
-    uint32_t ks = 0, kph = 0;                                        // K slot / phase
-    uint32_t vs = 1 % (uint32_t)stages, vph = 1 / (uint32_t)stages;  // V slot / phase
+    // ring slot / phase of the next load consumed: the ring holds K_g, V_{g-1},
+    // K_{g+1}, V_g, ... in the order of the MMAs below
+    uint32_t cs = 0, cph = 0;
+    auto consume = [&]() {
+      if (++cs == (uint32_t)stages) { cs = 0; cph ^= 1; }
+    };
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
     // the tile whose S has been issued but whose P V is still pending
     bool pend = false;
-    uint32_t pend_g = 0, pend_vs = 0, pend_vph = 0;
+    uint32_t pend_g = 0;
     int pend_ncols = 0;
     bool pend_first = false, pend_last = false;
 
     auto issue_pv = [&]() -> bool {
       if (!warp_wait(p_full, pend_g & 1)) return false;
-      if (!warp_wait(&kv_full[pend_vs], pend_vph)) return false;
+      if (!warp_wait(&kv_full[cs], cph)) return false;
       tc_fence_after();
       // A = P (TMEM, 8 columns per 16 keys), B = V (MN-major: d contiguous)
       const uint32_t p_tmem = tmem_base + kTmemS0 + (pend_g & 1) * kTmemSStride;
-      const uint64_t vd = vd0 + pend_vs * slot_step;
+      const uint64_t vd = vd0 + cs * slot_step;
       const uint32_t o_tmem = tmem_base + kTmemO;
       if (leader) {
         pv_group(pend_ncols >> 4, pend_first ? 0u : 1u, o_tmem, p_tmem, vd, idesc_pv);
-        umma_commit(&kv_empty[pend_vs]);
+        umma_commit(&kv_empty[cs]);
         umma_commit(pv_done);
         if (pend_last) umma_commit(o_full);
       }
       __syncwarp();
+      consume();
       return true;
     };
 
@@ -417,7 +451,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!warp_wait(&q_full[qbuf], (it >> 1) & 1)) { ok = false; break; }
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
         const Tile tl = tile_at(plan, bt, i, a.w, a.s);
-        if (!warp_wait(&kv_full[ks], kph)) { ok = false; break; }
+        if (!warp_wait(&kv_full[cs], cph)) { ok = false; break; }
         tc_fence_after();
         // S_g is issued before P V_{g-1} (which needs the softmax of tile g - 1),
         // also across blocks, so the tensor core computes S_g while the
@@ -426,7 +460,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // and tcgen05 MMAs of one thread execute in issue order.
         const uint32_t idesc_s = idesc_bf16_f32(128, tl.ncols, false);
         const uint32_t s_tmem = tmem_base + kTmemS0 + (g & 1) * kTmemSStride;
-        const uint64_t kd = kd0 + ks * slot_step;
+        const uint64_t kd = kd0 + cs * slot_step;
         if (leader) {
           umma_ss<0>(s_tmem, qd, kd, idesc_s);
 #pragma unroll
@@ -435,23 +469,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const uint32_t koff = (kk >> 2) * kvc16 + (kk & 3) * 2;
             umma_ss<1>(s_tmem, qd + qoff, kd + koff, idesc_s);
           }
-          umma_commit(&kv_empty[ks]);
+          umma_commit(&kv_empty[cs]);
           umma_commit(&s_full[g & 1]);
           if (a.sep_stage && i == bt.n_tiles - 1) umma_commit(&q_empty[qbuf]);
         }
         __syncwarp();
+        consume();
         if (pend && !issue_pv()) { ok = false; break; }
         pend = true;
         pend_g = g;
-        pend_vs = vs;
-        pend_vph = vph;
         pend_ncols = tl.ncols;
         pend_first = (i == 0);
         pend_last = (i == bt.n_tiles - 1);
-        ks += 2;
-        if (ks >= (uint32_t)stages) { ks -= stages; kph ^= 1; }
-        vs += 2;
-        if (vs >= (uint32_t)stages) { vs -= stages; vph ^= 1; }
       }
     }
     if (ok && pend) issue_pv();
