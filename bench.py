@@ -225,10 +225,12 @@ def launches_per_step(swa, cfg) -> int:
     return 1 + 1 + (2 if splits_ws else 1)
 
 
-def bench_decode(swa, device, stream, iters=64, warmup=8):
+def bench_decode(swa, device, stream, iters=64, warmup=8, pos=None):
     """Kernel-only decode at batch 64 over a rotating pool of distinct caches
     (> 4x L2), replayed as one CUDA graph of `ncache` decode launches."""
-    c = DECODE
+    c = dict(DECODE)
+    if pos is not None:
+        c["pos"] = pos
     B, Hq, Hkv, d, w, s = (c[x] for x in ("B", "Hq", "Hkv", "d", "w", "s"))
     kv_bytes = B * Hkv * (s + w) * d * 2 * 2
     ncache = max(8, int(math.ceil(4 * L2_BYTES / kv_bytes)))
@@ -258,6 +260,7 @@ def bench_decode(swa, device, stream, iters=64, warmup=8):
         e1.record(stream)
         e1.synchronize()
     ms_per_launch = e0.elapsed_time(e1) / (iters * ncache)
+    kv_bytes = B * Hkv * min(c["pos"] + 1, s + w) * d * 2 * 2  # slots actually read
     gbs = kv_bytes / (ms_per_launch * 1e-3) / 1e9
     return dict(kv_bytes_per_launch=kv_bytes, us_per_launch=ms_per_launch * 1e3, gbs=gbs,
                 caches=ncache, pool_bytes=ncache * kv_bytes)
@@ -373,6 +376,122 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return result
+
+
+# ------------------------------------------------------------------ other workloads
+# Supplementary measurements of the other configurations (one JSON line each);
+# the default workload above is the benchmark's step.
+
+def _time_events(fn, stream, iters, warmup=3):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def bench_window_sweep(swa, device, stream, peaks, iters=10):
+    """Long prefill window sweep: B=2, L=32768, Hq=32, Hkv=8, d=128, s=4,
+    w in {64, 256, 512}; inputs (1.3 GB) far exceed L2."""
+    B, L, Hq, Hkv, d, s = 2, 32768, 32, 8, 128, 4
+    q, k, v = (t.to(device) for t in swa_inputs.prefill_inputs(B, L, Hq, Hkv, d, 1004,
+                                                                 sink_rows=4))
+    out = torch.empty_like(q)
+    lines = []
+    for w in (64, 256, 512):
+        ms = _time_events(lambda: swa.swa_prefill(q, k, v, w, s, out=out), stream, iters)
+        fl = 4.0 * B * Hq * d * pairs_per_head(L, w, s)
+        by = B * L * (2 * Hq + 2 * Hkv) * d * 2
+        tf = fl / (ms * 1e-3) / 1e12
+        gbs = by / (ms * 1e-3) / 1e9
+        lines.append({"workload": f"prefill SWA({w},{s}) B={B} L={L} Hq={Hq} Hkv={Hkv} d={d}",
+                      "us_per_launch": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                      "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
+                      "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                      "inband_flop": fl, "algorithmic_bytes": by, "iters": iters})
+    return lines
+
+
+def bench_hybrid(swa, device, stream, peaks, n_layers=8, L=16384, steps=256):
+    """The hybrid stack: 8 layers alternating SWA(2048, 100) and full causal,
+    B=1, L=16384, Hq=32, Hkv=8, d=128: prefill of every layer, then `steps`
+    decode steps through all layers (one step captured as a CUDA graph)."""
+    B, Hq, Hkv, d = 1, 32, 8, 128
+    windows = swa.hybrid_layer_windows(n_layers, L, steps)
+    g = torch.Generator(device=device).manual_seed(1005)
+    qkv = [tuple(torch.randn(B, L, h, d, generator=g, device=device).to(torch.bfloat16)
+                 for h in (Hq, Hkv, Hkv)) for _ in range(n_layers)]
+    toks = [tuple(torch.randn(B, h, d, generator=g, device=device).to(torch.bfloat16)
+                  for h in (Hq, Hkv, Hkv)) for _ in range(n_layers)]
+    outs = [torch.empty(B, L, Hq, d, dtype=torch.bfloat16, device=device) for _ in range(n_layers)]
+
+    def prefill_all():
+        for (q, k, v), (w, s), o in zip(qkv, windows, outs):
+            swa.swa_prefill(q, k, v, w, s, out=o)
+
+    pre_ms = _time_events(prefill_all, stream, iters=3)
+    fl = sum(4.0 * B * Hq * d * pairs_per_head(L, w, s) for w, s in windows)
+    with torch.cuda.stream(stream):
+        stack = swa.HybridStack(B, Hq, Hkv, d, windows, device=device)
+        stack.prefill(qkv)
+        dec_out = stack.step(toks)            # first step: allocates workspaces
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            stack.step(toks, outs=dec_out)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps - 1):
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+    step_ms = e0.elapsed_time(e1) / (steps - 1)
+    # KV bytes one step reads: every slot each layer holds at the last position
+    kv = sum(B * Hkv * min(L + steps, s + w) * d * 2 * 2 for w, s in windows)
+    return [{"workload": f"hybrid stack {n_layers} layers (SWA(2048,100) / full causal) B={B} "
+                         f"L={L} Hq={Hq} Hkv={Hkv} d={d}",
+             "prefill_ms_all_layers": round(pre_ms, 3),
+             "prefill_tflops": round(fl / (pre_ms * 1e-3) / 1e12, 1),
+             "prefill_tensor_frac": round(fl / (pre_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+             "decode_us_per_step_all_layers": round(step_ms * 1e3, 2),
+             "decode_tokens_per_s": round(1e3 / step_ms, 1),
+             "decode_kv_gbs": round(kv / (step_ms * 1e-3) / 1e9, 1),
+             "decode_steps": steps}]
+
+
+def bench_decode_positions(swa, device, stream, peaks):
+    """Batch-64 decode at positions 128, 1K, 16K and 256K: the 68-slot cache
+    is full at each, so the bytes read (and the time) stay flat."""
+    lines = []
+    for pos in (128, 1024, 16384, 262143):
+        dec = bench_decode(swa, device, stream, pos=pos)
+        lines.append({"workload": f"{DECODE['name']}, pos={pos}",
+                      "us_per_launch": round(dec["us_per_launch"], 3),
+                      "kv_gbs": round(dec["gbs"], 1), "hbm_frac": round(dec["gbs"] / peaks["hbm_gbs"], 4),
+                      "kv_bytes_per_launch": dec["kv_bytes_per_launch"],
+                      "l2": f"{dec['caches']} distinct caches, {dec['pool_bytes'] / 1e6:.0f} MB"})
+    return lines
+
+
+def run_other(args):
+    import sliding_window_attention_05_b300 as swa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    fn = {"window-sweep": bench_window_sweep, "hybrid": bench_hybrid,
+          "decode-positions": bench_decode_positions}[args.workload]
+    for line in fn(swa, device, stream, peaks):
+        line["peak_source"] = peaks["source"]
+        print(json.dumps(line), flush=True)
 
 
 def run_e2e(swa, cfg, host, device, stream, K, world):
@@ -493,9 +612,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
+    ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions"),
+                    default="step", help="step (default): the benchmark line; the others print "
+                    "supplementary lines for the other configurations (1 GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload != "step" and args.impl == "ours":
+        run_other(args)
+        return
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -328,3 +328,7 @@ def swa_status_string(status: int) -> str:
 
 def swa_last_error() -> str:
     return _lib.swa_last_error().decode(errors="replace")
+
+
+# the hybrid attention stack driver (sequencing only; imports the names above)
+from .stack import AttentionLayer, HybridStack, hybrid_layer_windows  # noqa: E402,F401

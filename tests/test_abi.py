@@ -187,3 +187,15 @@ def test_schedule_skips_out_of_window_tiles():
     assert counts.numpy().max() == w + s
     visited = p["n_band"] * -(-(w + p["Tq"] - 1) // p["n_band"]) + p["s_box"]
     assert visited < 2 * (w + s)
+
+
+def test_hybrid_layer_windows():
+    """Even layers SWA(2048, 100); odd layers full causal, written as a window
+    that covers the prompt and every decode step, with no sinks."""
+    win = swa.hybrid_layer_windows(8, 16384, 256)
+    assert win[0::2] == [(2048, 100)] * 4
+    assert win[1::2] == [(16640, 0)] * 4
+    # a full-causal window never evicts: every position the run reaches keeps its slot
+    w, s = win[1]
+    slots = [swa.swa_cache_slot(p, w, s) for p in range(0, 16384 + 256, 97)]
+    assert slots == list(range(0, 16384 + 256, 97))

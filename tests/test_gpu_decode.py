@@ -152,40 +152,46 @@ def test_decode_group_sizes(Hq, Hkv, d):
 
 def test_hybrid_stack_prefill_then_decode():
     """8 layers alternating SWA(2048, 100) and full causal, B=1, L=16384,
-    Hq=32, Hkv=8, d=128; fresh seeded q/k/v per layer; prefill then 256
-    decode steps per layer. Sampled prefill rows and decode steps are checked."""
+    Hq=32, Hkv=8, d=128, through the package's HybridStack driver: fresh seeded
+    q/k/v per layer, prefill, then 256 decode steps through all layers (step by
+    step, as a decoder runs). Sampled prefill rows and decode steps of every
+    layer are checked against the oracle."""
     B, L, Hq, Hkv, d, steps = 1, 16384, 32, 8, 128, 256
     sc = scale_for(d)
     check_steps = {0, 1, 127, 255}
+    windows = swa.hybrid_layer_windows(8, L, steps)
+    assert windows[0] == (2048, 100) and windows[1] == (L + steps, 0)
+    host, toks = [], []
     for layer in range(8):
-        w, s = (2048, 100) if layer % 2 == 0 else (L + steps, 0)
         seed = 1000 + 5 * 100 + layer
         q, k, v = prefill_case(B, L, Hq, Hkv, d, seed)
         g = torch.Generator("cpu").manual_seed(seed + 77)
         qs = torch.randn(steps, B, Hq, d, generator=g).to(torch.bfloat16)
         ks = torch.randn(steps, B, 1, Hkv, d, generator=g).to(torch.bfloat16)
         vs = torch.randn(steps, B, 1, Hkv, d, generator=g).to(torch.bfloat16)
-        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-        out = swa.swa_prefill(qd, kd, vd, w, s, sc)
-        cache = swa.RingCache(B, Hkv, d, w, s)
-        cache.append(kd, vd)
-        dec = []
-        for i in range(steps):
-            cache.append(ks[i].cuda(), vs[i].cuda())
-            dec.append(cache.decode(qs[i].cuda(), sc))
-        torch.cuda.synchronize()
+        host.append((q, k, v, qs, ks, vs))
+        toks.append((qs.cuda(), ks[:, :, 0].cuda(), vs[:, :, 0].cuda()))
+    stack = swa.HybridStack(B, Hq, Hkv, d, windows, scale=sc)
+    outs = stack.prefill([(q.cuda(), k.cuda(), v.cuda()) for q, k, v, *_ in host])
+    dec = {}
+    for i in range(steps):
+        o = stack.step([(qs[i], ks[i], vs[i]) for qs, ks, vs in toks])
+        if i in check_steps:
+            dec[i] = [x.clone() for x in o]
+    torch.cuda.synchronize()
+    for layer, ((w, s), (q, k, v, qs, ks, vs)) in enumerate(zip(windows, host)):
         rng = np.random.default_rng(layer)
         rows = np.unique(np.concatenate([np.arange(64), np.arange(L - 16, L),
                                          rng.integers(0, L, 16)]))
         ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=rows)
-        compare(out[:, torch.from_numpy(rows).cuda()].cpu(), ref, f"layer {layer} prefill")
+        compare(outs[layer][:, torch.from_numpy(rows).cuda()].cpu(), ref, f"layer {layer} prefill")
         hist_k = torch.cat([k[0], ks[:, 0, 0]], 0)
         hist_v = torch.cat([v[0], vs[:, 0, 0]], 0)
         for i in sorted(check_steps):
             pos = L + i
             keys = oracle.keyset(pos, w, s)
             r, _ = oracle.decode(qs[i, 0], keys, hist_k[keys], hist_v[keys], pos, w, s, sc)
-            compare(dec[i][0].cpu(), r, f"layer {layer} decode step {i}")
+            compare(dec[i][layer][0].cpu(), r, f"layer {layer} decode step {i}")
 
 
 @pytest.mark.parametrize("case", [
