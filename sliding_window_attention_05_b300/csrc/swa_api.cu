@@ -204,12 +204,14 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
 
 // ------------------------------------------------------------------ decode
 
-// Query heads one decode CTA packs: the largest of 4, 2, 1 that divides G,
-// unless the (sequence, KV head) pairs are too few to fill the GPU; then one
-// head per CTA (the K/V rows shared by a group are read again from L2).
-int head_group(int B, int Hq, int Hkv) {
+// Query heads one decode CTA packs: the largest of 4, 2, 1 that divides G.
+// When the (sequence, KV head) pairs are too few to fill the GPU and the
+// cache is short (cap = s + w slots, too few to split), one head per CTA
+// instead: the K/V rows a group shares are then read again, from L2. A long
+// cache is split over CTAs instead, and every K/V row is read once.
+int head_group(int B, int Hq, int Hkv, long long cap) {
   const int G = Hq / Hkv;
-  if ((long long)B * Hkv * 2 < 148) return 1;
+  if ((long long)B * Hkv * 2 < 148 && cap <= 512) return 1;
   if (G % 4 == 0) return 4;
   if (G % 2 == 0) return 2;
   return 1;
@@ -221,8 +223,8 @@ int head_group(int B, int Hq, int Hkv) {
 // fixed from the capacity s + w (positions are only known on the device).
 int decode_splits(int B, int Hq, int Hkv, int w, int s) {
   const int G = Hq / Hkv;
-  const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv));
   const long long cap = (long long)s + w;
+  const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv, cap));
   long long sp = (cap + swa::kDecodeMaxKeys - 1) / swa::kDecodeMaxKeys;
   if (units < 148 && cap > 512) {
     long long fill = (296 + units - 1) / units;
@@ -266,7 +268,7 @@ cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream
 
 template <int D>
 cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
-  switch (head_group(B, a.Hq, a.Hkv)) {
+  switch (head_group(B, a.Hq, a.Hkv, (long long)a.w + a.s)) {
     case 4: return launch_decode_t<D, 4>(a, B, stream);
     case 2: return launch_decode_t<D, 2>(a, B, stream);
     default: return launch_decode_t<D, 1>(a, B, stream);
