@@ -255,39 +255,40 @@ class RingCache:
         self.B, self.Hkv, self.d, self.w, self.s = B, Hkv, d, w, s
         self.k = torch.zeros(B, Hkv, s + w, d, dtype=torch.bfloat16, device=device)
         self.v = torch.zeros_like(self.k)
+        # position the next appended token gets, per sequence (on the device, so
+        # that a CUDA graph of steps replays with advancing positions)
         self.next_pos = torch.zeros(B, dtype=torch.int32, device=device)
         self._last_pos = torch.zeros(B, dtype=torch.int32, device=device)
         self._workspace = None
+
+    def _workspace_for(self, q: torch.Tensor):
+        B, Hq, d = q.shape
+        need = swa_decode_workspace_size(B, Hq, self.Hkv, d, self.w, self.s)
+        if need and (self._workspace is None or self._workspace.numel() < need):
+            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        return self._workspace if need else None
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Append [B, T, Hkv, d] tokens after the ones already held."""
         T = k_new.shape[1]
         swa_cache_append(k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s, stream)
-        self._last_pos.copy_(self.next_pos + (T - 1))
         self.next_pos.add_(T)
 
     def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
              scale: float | None = None, out=None, stream=None):
         """Append one token per sequence (k_new/v_new [B, Hkv, d]) and decode
         q [B, Hq, d] at its position, in one launch."""
-        B, Hq, d = q.shape
-        need = swa_decode_workspace_size(B, Hq, self.Hkv, d, self.w, self.s)
-        if need and (self._workspace is None or self._workspace.numel() < need):
-            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-        self._last_pos.copy_(self.next_pos)
-        res = swa_append_decode(q, k_new, v_new, self.k, self.v, self._last_pos, self.w, self.s,
-                                scale, out, self._workspace if need else None, stream)
+        ws = self._workspace_for(q)
+        res = swa_append_decode(q, k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s,
+                                scale, out, ws, stream)
         self.next_pos.add_(1)
         return res
 
     def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):
         """Attend q [B, Hq, d] (the newest token's queries) over the cache."""
-        B, Hq, d = q.shape
-        need = swa_decode_workspace_size(B, Hq, self.Hkv, d, self.w, self.s)
-        if need and (self._workspace is None or self._workspace.numel() < need):
-            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-        return swa_decode(q, self.k, self.v, self._last_pos, self.w, self.s, scale, out,
-                          self._workspace if need else None, stream)
+        ws = self._workspace_for(q)
+        torch.sub(self.next_pos, 1, out=self._last_pos)
+        return swa_decode(q, self.k, self.v, self._last_pos, self.w, self.s, scale, out, ws, stream)
 
 
 # ---------------------------------------------------------------- test aids

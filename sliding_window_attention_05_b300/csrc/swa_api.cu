@@ -219,14 +219,19 @@ int head_group(int B, int Hq, int Hkv, long long cap) {
 
 // The cache of each (sequence, KV head) is split over CTAs when it holds
 // more slots than one CTA stages, or when there are too few (sequence, KV
-// head, head group) units to fill the GPU and the cache is long. The count is
-// fixed from the capacity s + w (positions are only known on the device).
+// head, head group) units to fill the GPU and the cache is long. In the
+// second case the splits hold at most 128 slots, so several CTAs share an SM
+// and one CTA's copies overlap another's arithmetic, and there are at least
+// two CTAs per SM where the cache allows 64 slots each. The count is fixed
+// from the capacity s + w (positions are only known on the device).
 int decode_splits(int B, int Hq, int Hkv, int w, int s) {
   const int G = Hq / Hkv;
   const long long cap = (long long)s + w;
   const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv, cap));
   long long sp = (cap + swa::kDecodeMaxKeys - 1) / swa::kDecodeMaxKeys;
   if (units < 148 && cap > 512) {
+    const long long fine = (cap + 127) / 128;
+    if (fine > sp) sp = fine;
     long long fill = (296 + units - 1) / units;
     const long long most = (cap + 63) / 64;
     if (fill > most) fill = most;
