@@ -43,6 +43,11 @@ WORKLOAD = dict(name="llama3.1-8b-layer-prefill+decode SWA(128,4)", B=1, L=4096,
 DECODE = dict(name="decode SWA(64,4) batch 64, 68-slot ring cache", B=64, Hq=32, Hkv=8, d=128,
               w=64, s=4, pos=262143)
 L2_BYTES = 126 * 1024 * 1024
+# DRAM bytes (read + write) of one launch of the prefill kernel on WORKLOAD,
+# from an ncu capture of the current kernel (dram__bytes_read.sum 50.43 MB +
+# dram__bytes_write.sum 2.05 MB). It describes that kernel only: it goes back
+# to None whenever the kernel changes, until a new capture is taken.
+PREFILL_TRAFFIC_BYTES = 52.48e6
 
 
 def pairs_per_head(L: int, w: int, s: int) -> int:
@@ -605,7 +610,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--traffic", type=float, default=None,
+    ap.add_argument("--traffic", type=float, default=PREFILL_TRAFFIC_BYTES,
                     help="DRAM bytes per prefill launch from an ncu capture of this kernel")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=24)
