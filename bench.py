@@ -486,6 +486,42 @@ def bench_decode_positions(swa, device, stream, peaks):
     return lines
 
 
+def bench_chunked(swa, device, stream, peaks, iters=5):
+    """Chunked prefill into the ring cache: the SWA(2048, 100) layer of the
+    hybrid stack (B=1, L=16384, Hq=32, Hkv=8, d=128) prefilled in chunks of
+    4096 and 1024, against the same prompt in one call."""
+    B, L, Hq, Hkv, d, w, s = 1, 16384, 32, 8, 128, 2048, 100
+    g = torch.Generator(device=device).manual_seed(1006)
+    q, k, v = (torch.randn(B, L, h, d, generator=g, device=device).to(torch.bfloat16)
+               for h in (Hq, Hkv, Hkv))
+    fl = 4.0 * B * Hq * d * pairs_per_head(L, w, s)
+    out = torch.empty_like(q)
+    lines = []
+    one = _time_events(lambda: swa.swa_prefill(q, k, v, w, s, out=out), stream, iters)
+    lines.append({"workload": f"prefill SWA({w},{s}) B={B} L={L} Hq={Hq} Hkv={Hkv} d={d}, one call",
+                  "ms": round(one, 4), "tflops": round(fl / (one * 1e-3) / 1e12, 1),
+                  "tensor_frac": round(fl / (one * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)})
+    for T in (4096, 1024):
+        with torch.cuda.stream(stream):
+            cache = swa.RingCache(B, Hkv, d, w, s, device=device)
+            chunks = [(q[:, p:p + T].contiguous(), k[:, p:p + T].contiguous(),
+                       v[:, p:p + T].contiguous(), out[:, p:p + T].contiguous())
+                      for p in range(0, L, T)]
+
+        def run():
+            cache.next_pos.zero_()
+            cache.length = 0
+            for qc, kc, vc, oc in chunks:
+                cache.prefill_chunk(qc, kc, vc, out=oc)
+
+        ms = _time_events(run, stream, iters)
+        lines.append({"workload": f"chunked prefill SWA({w},{s}) B={B} L={L} in chunks of {T}",
+                      "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                      "tensor_frac": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                      "vs_one_call": round(one / ms, 3)})
+    return lines
+
+
 def run_other(args):
     import sliding_window_attention_05_b300 as swa
     device = torch.device("cuda", 0)
@@ -493,7 +529,7 @@ def run_other(args):
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
     fn = {"window-sweep": bench_window_sweep, "hybrid": bench_hybrid,
-          "decode-positions": bench_decode_positions}[args.workload]
+          "decode-positions": bench_decode_positions, "chunked": bench_chunked}[args.workload]
     for line in fn(swa, device, stream, peaks):
         line["peak_source"] = peaks["source"]
         print(json.dumps(line), flush=True)
@@ -617,7 +653,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
-    ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions"),
+    ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions",
+                                           "chunked"),
                     default="step", help="step (default): the benchmark line; the others print "
                     "supplementary lines for the other configurations (1 GPU)")
     args = ap.parse_args(argv)

@@ -85,6 +85,32 @@ SWA_API int swa_cache_append(const void *k_new, const void *v_new, void *kcache,
                      const int *pos_start, int B, int T, int Hkv, int d, int w, int s,
                      swa_stream_t stream);
 
+/* Chunked prefill into a ring cache: the T prompt tokens at positions
+ * pos0 .. pos0 + T - 1 of every sequence (one pos0 for the whole batch) attend
+ * over the keys the cache still holds plus the chunk's own keys, and are then
+ * appended to the cache. Row i of out equals row pos0 + i of swa_prefill over
+ * the whole prompt (wiblog.cn long-context SWA article, section
+ * "长 Prompt 的分块处理与工程实现": a long prompt is prefilled in pieces while
+ * the rolling cache fills).
+ *   q [B, T, Hq, d]; k_new, v_new [B, T, Hkv, d]; out [B, T, Hq, d] (written)
+ *   kcache, vcache [B, Hkv, s + w, d]: every position < pos0 must already have
+ *   been appended (swa_cache_append, swa_append_decode or earlier chunks). The
+ *   rows a chunk needs from before pos0 are the sinks and the last w - 1
+ *   positions, which the ring keeps.
+ *   workspace: caller-owned device memory of at least
+ *   swa_prefill_chunk_workspace_size(...) bytes, 16-byte aligned; its size grows
+ *   with (min(pos0, s + w - 1) + T) rows of q, k, v and out.
+ * The work: a staging kernel lays the kept cache rows and the chunk out
+ * contiguously in the workspace, the prefill kernel runs over the query blocks
+ * that hold chunk rows, a copy kernel writes the chunk's rows to out, and the
+ * append kernel stores the chunk. */
+SWA_API size_t swa_prefill_chunk_workspace_size(int B, int T, int Hq, int Hkv, int d, int w, int s,
+                                                long long pos0);
+SWA_API int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kcache,
+                              void *vcache, void *out, int B, int T, int Hq, int Hkv, int d, int w,
+                              int s, long long pos0, float scale, void *workspace,
+                              size_t workspace_bytes, swa_stream_t stream);
+
 /* Bytes of device workspace swa_decode needs for these sizes (0 if none). */
 SWA_API size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s);
 

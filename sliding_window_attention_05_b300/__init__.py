@@ -51,6 +51,11 @@ _lib.swa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
 _lib.swa_append_decode.restype = _i
 _lib.swa_append_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
                                    _vp, _sz, _vp]
+_lib.swa_prefill_chunk_workspace_size.restype = _sz
+_lib.swa_prefill_chunk_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.c_longlong]
+_lib.swa_prefill_chunk.restype = _i
+_lib.swa_prefill_chunk.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                   ctypes.c_longlong, _f, _vp, _sz, _vp]
 _lib.swa_decode_noalloc.restype = _i
 _lib.swa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.swa_cache_slot.restype = ctypes.c_longlong
@@ -241,7 +246,39 @@ def swa_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     return out
 
 
+def swa_prefill_chunk_workspace_size(B: int, T: int, Hq: int, Hkv: int, d: int, w: int, s: int,
+                                     pos0: int) -> int:
+    return int(_lib.swa_prefill_chunk_workspace_size(B, T, Hq, Hkv, d, w, s, int(pos0)))
+
+
+def swa_prefill_chunk(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      kcache: torch.Tensor, vcache: torch.Tensor, pos0: int, w: int, s: int,
+                      scale: float | None = None, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """Prefill the chunk q [B,T,Hq,d], k_new/v_new [B,T,Hkv,d] at positions
+    pos0 .. pos0+T-1 against the ring cache, then append it; returns out [B,T,Hq,d]."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
+                 (vcache, "vcache")):
+        _bf16_cuda(t, n)
+    B, T, Hq, d = q.shape
+    Hkv = kcache.shape[1]
+    if k_new.shape != (B, T, Hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new/v_new must be [B, T, Hkv, d] = {(B, T, Hkv, d)}")
+    if out is None:
+        out = torch.empty_like(q)
+    need = swa_prefill_chunk_workspace_size(B, T, Hq, Hkv, d, w, s, pos0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.swa_prefill_chunk(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                                  _ptr(out), B, T, Hq, Hkv, d, int(w), int(s), int(pos0),
+                                  _default_scale(d, scale), _ptr(workspace), wbytes,
+                                  _stream(stream)), "swa_prefill_chunk")
+    return out
+
+
 cache_append = swa_cache_append
+prefill_chunk = swa_prefill_chunk
 decode = swa_decode
 append_decode = swa_append_decode
 
@@ -260,6 +297,10 @@ class RingCache:
         self.next_pos = torch.zeros(B, dtype=torch.int32, device=device)
         self._last_pos = torch.zeros(B, dtype=torch.int32, device=device)
         self._workspace = None
+        self._chunk_ws = None
+        # host copy of next_pos for the chunked prefill (which needs pos0 on the
+        # host); every method below keeps both in step
+        self.length = 0
 
     def _workspace_for(self, q: torch.Tensor):
         B, Hq, d = q.shape
@@ -273,6 +314,21 @@ class RingCache:
         T = k_new.shape[1]
         swa_cache_append(k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s, stream)
         self.next_pos.add_(T)
+        self.length += T
+
+    def prefill_chunk(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      scale: float | None = None, out=None, stream=None):
+        """Attention of the next T prompt tokens (q [B,T,Hq,d], k_new/v_new
+        [B,T,Hkv,d]) over the cache plus themselves; the chunk is then appended."""
+        B, T, Hq, d = q.shape
+        need = swa_prefill_chunk_workspace_size(B, T, Hq, self.Hkv, d, self.w, self.s, self.length)
+        if self._chunk_ws is None or self._chunk_ws.numel() < need:
+            self._chunk_ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        res = swa_prefill_chunk(q, k_new, v_new, self.k, self.v, self.length, self.w, self.s,
+                                scale, out, self._chunk_ws, stream)
+        self.next_pos.add_(T)
+        self.length += T
+        return res
 
     def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
              scale: float | None = None, out=None, stream=None):
@@ -282,6 +338,7 @@ class RingCache:
         res = swa_append_decode(q, k_new, v_new, self.k, self.v, self.next_pos, self.w, self.s,
                                 scale, out, ws, stream)
         self.next_pos.add_(1)
+        self.length += 1
         return res
 
     def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/swa.h"
+#include "chunk.cuh"
 #include "decode.cuh"
 #include "prefill.cuh"
 #include "sm100_ptx.cuh"
@@ -149,10 +150,13 @@ size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages, bool 
                  : swa::PrefillSmem<128>::bytes(plan, stages, sep);
 }
 
+// qb_first: query blocks below it are skipped (their rows of out are left
+// unwritten). Work items run from the last query block down, so dropping the
+// tail of the item range drops exactly those blocks.
 template <int D>
 int launch_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
                    int Hkv, int w, int s, float scale, cudaStream_t stream,
-                   const DeviceInfo &dev) {
+                   const DeviceInfo &dev, int qb_first = 0) {
   const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
   CUtensorMap tq, tk, tv, tks, tvs, to;
   int rc;
@@ -190,7 +194,7 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.s = s;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.plan = plan;
-  a.n_items = B * Hkv * plan.nqb;
+  a.n_items = B * Hkv * (plan.nqb - qb_first);
   a.stages = stages;
   a.kv_chunk = swa::PrefillSmem<D>::chunk_bytes(plan);
   a.sep_stage = sep_stage ? 1 : 0;
@@ -318,6 +322,27 @@ int noalloc_scratch_ptr(void **out) {
   return SWA_OK;
 }
 
+// Device workspace of swa_prefill_chunk: the append's positions, then the
+// staged q, k, v and the prefill output over the prefix + chunk rows.
+struct ChunkWorkspace {
+  size_t pos, qx, kx, vx, ox, total;
+};
+
+ChunkWorkspace chunk_workspace(int B, int T, int Hq, int Hkv, int d, int w, int s,
+                               long long pos0) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t Lx = (size_t)(swa::chunk_prefix_rows(pos0, w, s) + T);
+  const size_t qb = up((size_t)B * Lx * Hq * d * 2), kvb = up((size_t)B * Lx * Hkv * d * 2);
+  ChunkWorkspace c;
+  c.pos = 0;
+  c.qx = up((size_t)B * sizeof(int));
+  c.kx = c.qx + qb;
+  c.vx = c.kx + kvb;
+  c.ox = c.vx + kvb;
+  c.total = c.ox + qb;
+  return c;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -424,6 +449,80 @@ int swa_cache_append(const void *k_new, const void *v_new, void *kcache, void *v
       reinterpret_cast<uint4 *>(vcache), pos_start, T, Hkv, d, w, s, max_surv);
   if (e != cudaSuccess) return cuda_fail(e, "swa_cache_append launch");
   return SWA_OK;
+}
+
+size_t swa_prefill_chunk_workspace_size(int B, int T, int Hq, int Hkv, int d, int w, int s,
+                                        long long pos0) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || pos0 < 0 ||
+      !supported_d(d))
+    return 0;
+  return chunk_workspace(B, T, Hq, Hkv, d, w, s, pos0).total;
+}
+
+int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kcache,
+                      void *vcache, void *out, int B, int T, int Hq, int Hkv, int d, int w, int s,
+                      long long pos0, float scale, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream) {
+  if (!q || !k_new || !v_new || !kcache || !vcache || !out)
+    return fail(SWA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kcache) ||
+      !aligned16(vcache) || !aligned16(out) || !aligned16(workspace))
+    return fail(SWA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (B < 1 || T < 1) return fail(SWA_ERR_INVALID_ARG, "B and T must be >= 1");
+  if (w < 1) return fail(SWA_ERR_INVALID_ARG, "window w must be >= 1");
+  if (s < 0) return fail(SWA_ERR_INVALID_ARG, "sink count s must be >= 0");
+  if (pos0 < 0) return fail(SWA_ERR_INVALID_ARG, "pos0 must be >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if ((rc = check_scale(scale))) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if (pos0 + T > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "positions beyond int32");
+  if (B > 65535) return fail(SWA_ERR_UNSUPPORTED, "B > 65535");
+  const ChunkWorkspace ws = chunk_workspace(B, T, Hq, Hkv, d, w, s, pos0);
+  if (!workspace || workspace_bytes < ws.total)
+    return fail(SWA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, ws.total);
+  const int n_pre = (int)swa::chunk_prefix_rows(pos0, w, s);
+  const int Lx = n_pre + T;
+  const int Tq = 128 / (Hq / Hkv);  // query positions per prefill block
+  if ((long long)B * Hkv * swa::cdiv(Lx, 128 / (Hq / Hkv)) > 0x7FFFFFFFll)
+    return fail(SWA_ERR_UNSUPPORTED, "too many query blocks");
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *base = reinterpret_cast<uint8_t *>(workspace);
+  int *wpos = reinterpret_cast<int *>(base + ws.pos);
+  void *qx = base + ws.qx, *kx = base + ws.kx, *vx = base + ws.vx, *ox = base + ws.ox;
+
+  // 1. stage [kept cache rows | chunk] contiguously
+  const int threads = 256;
+  long long n = (long long)Lx * (Hq + 2 * Hkv) * (d / 8);
+  if (n < B) n = B;
+  long long blocks = (n + threads - 1) / threads;
+  if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "chunk too large");
+  cudaError_t e = launch_pdl(
+      swa::swa_chunk_stage_kernel, dim3((unsigned)blocks, B), dim3(threads), 0, st,
+      reinterpret_cast<const uint4 *>(q), reinterpret_cast<const uint4 *>(k_new),
+      reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<const uint4 *>(kcache),
+      reinterpret_cast<const uint4 *>(vcache), reinterpret_cast<uint4 *>(qx),
+      reinterpret_cast<uint4 *>(kx), reinterpret_cast<uint4 *>(vx), wpos, B, T, Hq, Hkv, d, w, s,
+      pos0, n_pre, (n_pre / Tq) * Tq);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_chunk stage launch");
+  // 2. the prefill kernel over the staged rows
+  // (query blocks made only of prefix rows are skipped)
+  const int qb_first = n_pre / Tq;
+  rc = d == 64 ? launch_prefill<64>(qx, kx, vx, ox, B, Lx, Hq, Hkv, w, s, scale, st, dev, qb_first)
+               : launch_prefill<128>(qx, kx, vx, ox, B, Lx, Hq, Hkv, w, s, scale, st, dev, qb_first);
+  if (rc) return rc;
+  // 3. the chunk's rows to out
+  n = (long long)T * Hq * (d / 8);
+  blocks = (n + threads - 1) / threads;
+  e = launch_pdl(swa::swa_chunk_out_kernel, dim3((unsigned)blocks, B), dim3(threads), 0, st,
+                 reinterpret_cast<const uint4 *>(ox), reinterpret_cast<uint4 *>(out), T, Hq, d,
+                 n_pre);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_chunk output launch");
+  // 4. append the chunk (after the staging read every cache row it needs)
+  return swa_cache_append(k_new, v_new, kcache, vcache, wpos, B, T, Hkv, d, w, s, stream);
 }
 
 size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {

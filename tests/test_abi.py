@@ -199,3 +199,38 @@ def test_hybrid_layer_windows():
     w, s = win[1]
     slots = [swa.swa_cache_slot(p, w, s) for p in range(0, 16384 + 256, 97)]
     assert slots == list(range(0, 16384 + 256, 97))
+
+
+def test_prefill_chunk_rejects_bad_arguments():
+    lib = swa.lib()
+    dummy = ctypes.c_void_p(4096)
+    args = dict(B=1, T=64, Hq=8, Hkv=2, d=64, w=32, s=4, pos0=100)
+
+    def call(ws=dummy, nbytes=1 << 30, **kw):
+        a = dict(args, **kw)
+        return lib.swa_prefill_chunk(dummy, dummy, dummy, dummy, dummy, dummy, a["B"], a["T"],
+                                     a["Hq"], a["Hkv"], a["d"], a["w"], a["s"], a["pos0"],
+                                     ctypes.c_float(0.125), ws, nbytes, None)
+
+    assert call(pos0=-1) == swa.SWA_ERR_INVALID_ARG
+    assert call(T=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(w=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(Hq=7) == swa.SWA_ERR_INVALID_ARG
+    assert call(d=96) == swa.SWA_ERR_UNSUPPORTED
+    need = swa.swa_prefill_chunk_workspace_size(1, 64, 8, 2, 64, 32, 4, 100)
+    assert call(nbytes=need - 1) == swa.SWA_ERR_INVALID_ARG
+    assert "workspace" in swa.swa_last_error()
+    assert call(ws=None) == swa.SWA_ERR_INVALID_ARG
+
+
+def test_prefill_chunk_workspace_size():
+    """q, k, v and out over min(pos0, s + w - 1) + T staged rows, plus the
+    append's positions: it stops growing once pos0 passes s + w - 1."""
+    f = swa.swa_prefill_chunk_workspace_size
+    assert f(1, 64, 8, 2, 64, 32, 4, -1) == 0
+    assert f(1, 64, 8, 2, 64, 0, 4, 0) == 0
+    row = (2 * 8 + 2 * 2) * 64 * 2          # bytes of one staged row of q, out, k, v
+    a, b = f(1, 64, 8, 2, 64, 32, 4, 0), f(1, 64, 8, 2, 64, 32, 4, 35)
+    assert b - a == 35 * row
+    assert f(1, 64, 8, 2, 64, 32, 4, 10_000) == f(1, 64, 8, 2, 64, 32, 4, 35)
+    assert a >= 64 * row
