@@ -309,6 +309,12 @@ class RingCache:
             self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         return self._workspace if need else None
 
+    def seek(self, pos: int):
+        """Make pos the position the next appended token gets, for every
+        sequence (e.g. to fill only the slots a later position still needs)."""
+        self.next_pos.fill_(int(pos))
+        self.length = int(pos)
+
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Append [B, T, Hkv, d] tokens after the ones already held."""
         T = k_new.shape[1]

@@ -99,7 +99,7 @@ def test_batch64_decode_positions(P):
     lo = max(s, P - w + 1)
     win = np.arange(lo, P + 1)
     # jump: the window part starts at lo, not at s
-    cache.next_pos.fill_(lo)
+    cache.seek(lo)
     cache.append(_keyed(seed, 0, B, Hkv, win, d).cuda(), _keyed(seed, 1, B, Hkv, win, d).cuda())
     for step in range(1, 4):
         pos = P + step
