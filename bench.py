@@ -522,6 +522,55 @@ def bench_chunked(swa, device, stream, peaks, iters=5):
     return lines
 
 
+def bench_paged_decode(swa, device, stream, peaks, iters=64, page_size=64):
+    """Batch-64 decode, SWA(64, 4), through the paged layout (pages of 64
+    positions: the sink page and the two window pages at position 262143),
+    over a rotating set of caches drawn from one pool (> 4x L2)."""
+    c = DECODE
+    B, Hq, Hkv, d, w, s, pos = (c[x] for x in ("B", "Hq", "Hkv", "d", "w", "s", "pos"))
+    kv_bytes = B * Hkv * (s + w) * d * 2 * 2
+    ncache = max(8, int(math.ceil(4 * L2_BYTES / kv_bytes)))
+    pages_per_seq = 3
+    pool = swa.PagePool(ncache * B * pages_per_seq, Hkv, d, page_size=page_size, device=device)
+    g = torch.Generator(device=device).manual_seed(1007)
+    pool.k.copy_(torch.randn(pool.k.shape, generator=g, device=device).to(torch.bfloat16))
+    pool.v.copy_(torch.randn(pool.v.shape, generator=g, device=device).to(torch.bfloat16))
+    caches = []
+    for _ in range(ncache):
+        pc = swa.PagedKVCache(pool, B, w, s, max_len=pos + 1)
+        pc._reserve(pos)
+        pc.length = pos + 1
+        caches.append(pc)
+    q = torch.randn(B, Hq, d, generator=g, device=device).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    with torch.cuda.stream(stream):
+        for pc in caches:            # sets every cache's position outside the graph
+            pc.decode(q, out=out)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for pc in caches:
+                pc.decode(q, out=out)
+        for _ in range(8):
+            graph.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+    us = e0.elapsed_time(e1) / (iters * ncache) * 1e3
+    gbs = kv_bytes / (us * 1e-6) / 1e9
+    ring = bench_decode(swa, device, stream)
+    return [{"workload": f"paged decode SWA({w},{s}) batch {B}, pages of {page_size}, pos={pos}",
+             "us_per_launch": round(us, 3), "kv_gbs": round(gbs, 1),
+             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "kv_bytes_per_launch": kv_bytes,
+             "ring_us_per_launch": round(ring["us_per_launch"], 3),
+             "l2": f"{ncache} caches in one pool of {pool.n_pages} pages"}]
+
+
 def run_other(args):
     import sliding_window_attention_05_b300 as swa
     device = torch.device("cuda", 0)
@@ -529,7 +578,8 @@ def run_other(args):
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
     fn = {"window-sweep": bench_window_sweep, "hybrid": bench_hybrid,
-          "decode-positions": bench_decode_positions, "chunked": bench_chunked}[args.workload]
+          "decode-positions": bench_decode_positions, "chunked": bench_chunked,
+          "paged-decode": bench_paged_decode}[args.workload]
     for line in fn(swa, device, stream, peaks):
         line["peak_source"] = peaks["source"]
         print(json.dumps(line), flush=True)
@@ -654,7 +704,7 @@ def main(argv=None):
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
     ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions",
-                                           "chunked"),
+                                           "chunked", "paged-decode"),
                     default="step", help="step (default): the benchmark line; the others print "
                     "supplementary lines for the other configurations (1 GPU)")
     args = ap.parse_args(argv)

@@ -167,6 +167,58 @@ SWA_API int swa_decode_noalloc(const void *q, const void *kcache, const void *vc
                                const int *pos, void *out, int B, int Hq, int Hkv, int d, int w,
                                int s, float scale, swa_stream_t stream);
 
+/* ------------------------------------------------------------------ paged layout
+ * K and V of every layer can instead live in pages of page_size positions drawn
+ * from one pool: kpool, vpool [n_pages, Hkv, page_size, d] bf16 (DEVICE, the
+ * caller's). A sequence's page table, int32 [max_pages], maps logical page lp
+ * (positions lp * page_size .. lp * page_size + page_size - 1) to a physical
+ * page, or -1. A layer with window w and s sinks keeps exactly the pages that
+ * hold a position of K(p): sliding-window layers recycle theirs as the window
+ * moves, full-attention layers (w beyond every position) keep growing
+ * ("Hybrid Sliding Window Attention (Hybrid SWA)", section
+ * "三、1. vLLM 中的 Hybrid KV Cache 最佳实践"; the SWA(w, s) explainer, section
+ * "工程落地与实践" item 1, route B: cache only the last w tokens and the sinks).
+ * The page pool and the tables are HOST objects; the caller copies each table
+ * to the device before a launch that reads it. */
+typedef struct swa_page_pool swa_page_pool;
+
+/* A pool of n_pages physical pages, all free. NULL on n_pages < 1. */
+SWA_API swa_page_pool *swa_page_pool_create(int n_pages);
+SWA_API void swa_page_pool_destroy(swa_page_pool *pool);
+/* Free pages left in the pool (-1 for NULL). Thread-safe. */
+SWA_API int swa_page_pool_free_pages(swa_page_pool *pool);
+
+/* Prepare one sequence's HOST page table (int32 [max_pages], -1 = unmapped,
+ * all -1 for a new sequence) for appending positions up to pos_hi and attending
+ * at pos_hi: pages are taken from the pool for every logical page holding a
+ * position of K(pos_hi) that is unmapped, and mapped pages that hold none are
+ * returned. Call it with non-decreasing pos_hi. SWA_ERR_UNSUPPORTED (nothing
+ * changed) when the pool has too few free pages or pos_hi lies beyond the
+ * table; SWA_ERR_INVALID_ARG for a table entry this pool did not hand out.
+ * Thread-safe per pool; the table is the caller's. */
+SWA_API int swa_paged_reserve(swa_page_pool *pool, int *table, int max_pages, long long pos_hi,
+                              int w, int s, int page_size);
+/* Return every page of a table to the pool and unmap it (end of a sequence). */
+SWA_API int swa_paged_release(swa_page_pool *pool, int *table, int max_pages);
+
+/* Paged swa_cache_append: the same survivors, stored in the pages of
+ * page_table (DEVICE int32 [B, max_pages], prepared by swa_paged_reserve for the
+ * last position of the call); n_pages is the pools' page count. An unmapped or
+ * out-of-range page is skipped and flagged in the device error word. */
+SWA_API int swa_paged_append(const void *k_new, const void *v_new, void *kpool, void *vpool,
+                             const int *page_table, const int *pos_start, int B, int T, int Hkv,
+                             int d, int page_size, int max_pages, int n_pages, int w, int s,
+                             swa_stream_t stream);
+/* Paged swa_decode: the same result, reading K(pos[b]) through page_table
+ * (DEVICE int32 [B, max_pages]); workspace as swa_decode_workspace_size. A CTA
+ * that meets an unmapped or out-of-range page issues no copy, writes nothing
+ * and flags the device error word. */
+SWA_API int swa_paged_decode(const void *q, const void *kpool, const void *vpool,
+                             const int *page_table, const int *pos, void *out, int B, int Hq,
+                             int Hkv, int d, int page_size, int max_pages, int n_pages, int w,
+                             int s, float scale, void *workspace, size_t workspace_bytes,
+                             swa_stream_t stream);
+
 /* Host helper: the cache slot of position pos (the formula above), or -1 for
  * pos < 0, w < 1 or s < 0. */
 SWA_API long long swa_cache_slot(long long pos, int w, int s);

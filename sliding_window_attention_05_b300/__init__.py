@@ -56,6 +56,22 @@ _lib.swa_prefill_chunk_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i, ct
 _lib.swa_prefill_chunk.restype = _i
 _lib.swa_prefill_chunk.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                    ctypes.c_longlong, _f, _vp, _sz, _vp]
+_lib.swa_page_pool_create.restype = _vp
+_lib.swa_page_pool_create.argtypes = [_i]
+_lib.swa_page_pool_destroy.restype = None
+_lib.swa_page_pool_destroy.argtypes = [_vp]
+_lib.swa_page_pool_free_pages.restype = _i
+_lib.swa_page_pool_free_pages.argtypes = [_vp]
+_lib.swa_paged_reserve.restype = _i
+_lib.swa_paged_reserve.argtypes = [_vp, _vp, _i, ctypes.c_longlong, _i, _i, _i]
+_lib.swa_paged_release.restype = _i
+_lib.swa_paged_release.argtypes = [_vp, _vp, _i]
+_lib.swa_paged_append.restype = _i
+_lib.swa_paged_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                  _i, _vp]
+_lib.swa_paged_decode.restype = _i
+_lib.swa_paged_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                  _f, _vp, _sz, _vp]
 _lib.swa_decode_noalloc.restype = _i
 _lib.swa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.swa_cache_slot.restype = ctypes.c_longlong
@@ -352,6 +368,114 @@ class RingCache:
         ws = self._workspace_for(q)
         torch.sub(self.next_pos, 1, out=self._last_pos)
         return swa_decode(q, self.k, self.v, self._last_pos, self.w, self.s, scale, out, ws, stream)
+
+
+# ---------------------------------------------------------------- paged layout
+
+class PagePool:
+    """A pool of KV pages shared by layers: the host allocator (in libswa.so)
+    and the device pools kpool, vpool [n_pages, Hkv, page_size, d] bf16."""
+
+    def __init__(self, n_pages: int, Hkv: int, d: int, page_size: int = 64, device=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        handle = _lib.swa_page_pool_create(n_pages)
+        if not handle:
+            raise SwaError(SWA_ERR_INVALID_ARG, "swa_page_pool_create")
+        self._h = ctypes.c_void_p(handle)
+        self.n_pages, self.Hkv, self.d, self.page_size = n_pages, Hkv, d, page_size
+        self.k = torch.zeros(n_pages, Hkv, page_size, d, dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros_like(self.k)
+
+    def free_pages(self) -> int:
+        return int(_lib.swa_page_pool_free_pages(self._h))
+
+    def reserve(self, table, pos_hi: int, w: int, s: int):
+        """table: host int32 tensor [max_pages] (contiguous)."""
+        _check(_lib.swa_paged_reserve(self._h, ctypes.c_void_p(table.data_ptr()), table.numel(),
+                                      int(pos_hi), int(w), int(s), self.page_size),
+               "swa_paged_reserve")
+
+    def release(self, table):
+        _check(_lib.swa_paged_release(self._h, ctypes.c_void_p(table.data_ptr()), table.numel()),
+               "swa_paged_release")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.swa_page_pool_destroy(h)
+            self._h = None
+
+
+class PagedKVCache:
+    """One layer's KV cache in the pages of a shared PagePool: SWA(w, s)
+    layers keep the pages of the sinks and the last w positions, full layers
+    (w beyond every position) keep every page. Positions advance together for
+    the B sequences; the page tables are kept on the host and copied to the
+    device whenever they change."""
+
+    def __init__(self, pool: PagePool, B: int, w: int, s: int, max_len: int):
+        self.pool, self.B, self.w, self.s = pool, B, w, s
+        self.max_pages = (max_len + pool.page_size - 1) // pool.page_size
+        # pageable on purpose: a copy from it takes its contents at the call,
+        # so the next step's reserve cannot change what this step's kernels see
+        self.table = torch.full((B, self.max_pages), -1, dtype=torch.int32)
+        device = pool.k.device
+        self.table_dev = torch.full((B, self.max_pages), -1, dtype=torch.int32, device=device)
+        self.length = 0
+        self.pos_dev = torch.zeros(B, dtype=torch.int32, device=device)
+        self._pos_value = 0          # what pos_dev holds (set only when it changes)
+        self._workspace = None
+
+    def _set_pos(self, value: int):
+        if value != self._pos_value:
+            self.pos_dev.fill_(value)
+            self._pos_value = value
+
+    def _reserve(self, pos_hi: int):
+        for b in range(self.B):
+            self.pool.reserve(self.table[b], pos_hi, self.w, self.s)
+        self.table_dev.copy_(self.table)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """Append [B, T, Hkv, d] tokens at positions length .. length + T - 1."""
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _bf16_cuda(t, n)
+        B, T, Hkv, d = k_new.shape
+        self._reserve(self.length + T - 1)
+        self._set_pos(self.length)
+        _check(_lib.swa_paged_append(_ptr(k_new), _ptr(v_new), _ptr(self.pool.k), _ptr(self.pool.v),
+                                     _ptr(self.table_dev), _ptr(self.pos_dev), B, T, Hkv, d,
+                                     self.pool.page_size, self.max_pages, self.pool.n_pages,
+                                     self.w, self.s, _stream(stream)), "swa_paged_append")
+        self.length += T
+
+    def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):
+        """q [B, Hq, d]: attend at the newest position (length - 1)."""
+        _bf16_cuda(q, "q")
+        B, Hq, d = q.shape
+        need = swa_decode_workspace_size(B, Hq, self.pool.Hkv, d, self.w, self.s)
+        if need and (self._workspace is None or self._workspace.numel() < need):
+            self._workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws = self._workspace if need else None
+        if out is None:
+            out = torch.empty_like(q)
+        self._set_pos(self.length - 1)
+        wbytes = 0 if ws is None else ws.numel()
+        _check(_lib.swa_paged_decode(_ptr(q), _ptr(self.pool.k), _ptr(self.pool.v),
+                                     _ptr(self.table_dev), _ptr(self.pos_dev), _ptr(out), B, Hq,
+                                     self.pool.Hkv, d, self.pool.page_size, self.max_pages,
+                                     self.pool.n_pages, self.w, self.s, _default_scale(d, scale),
+                                     _ptr(ws), wbytes, _stream(stream)), "swa_paged_decode")
+        return out
+
+    def pages_held(self) -> int:
+        return int((self.table >= 0).sum())
+
+    def release(self):
+        for b in range(self.B):
+            self.pool.release(self.table[b])
+        self.table_dev.fill_(-1)
+        self.length = 0
 
 
 # ---------------------------------------------------------------- test aids

@@ -62,6 +62,49 @@ __global__ void swa_append_kernel(const uint4 *__restrict__ k_new, const uint4 *
   vcache[dst] = v_new[src];
 }
 
+// Paged form of the append: the same survivors, written to row p % page_size
+// of the physical page table[b][p / page_size] of the pools
+// [n_pages, Hkv, page_size, d]. An unmapped (or out-of-range) page is skipped
+// and flagged.
+__global__ void swa_paged_append_kernel(const uint4 *__restrict__ k_new,
+                                        const uint4 *__restrict__ v_new, uint4 *__restrict__ kpool,
+                                        uint4 *__restrict__ vpool, const int *__restrict__ table,
+                                        const int *__restrict__ pos_start, int T, int Hkv, int d,
+                                        int w, int s, int max_survivors, int page_size,
+                                        int max_pages, int n_pages) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int b = blockIdx.y;
+  const int vec_per_row = d / 8;
+  const long long n = (long long)max_survivors * Hkv * vec_per_row;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n) return;
+  const int c = (int)(idx % vec_per_row);
+  const int kvh = (int)((idx / vec_per_row) % Hkv);
+  const int k = (int)(idx / ((long long)vec_per_row * Hkv));
+  const int p0 = pos_start[b];
+  if (p0 < 0) {
+    if (idx == 0) record_error(kErrNegativePosition);
+    return;
+  }
+  const int h = imin(imax(s - p0, 0), T);
+  const int tail0 = imax(h, T - w);
+  const int i = k < h ? k : tail0 + (k - h);
+  if (i >= T) return;
+  const long long p = (long long)p0 + i;
+  const long long lp = p / page_size;
+  const int page = lp < max_pages ? table[(long long)b * max_pages + lp] : -1;
+  if (page < 0 || page >= n_pages) {
+    record_error(kErrMissingPage);
+    return;
+  }
+  const long long src = (((long long)b * T + i) * Hkv + kvh) * vec_per_row + c;
+  const long long dst =
+      (((long long)page * Hkv + kvh) * page_size + p % page_size) * vec_per_row + c;
+  kpool[dst] = k_new[src];
+  vpool[dst] = v_new[src];
+}
+
 // ---------------------------------------------------------------- decode
 
 constexpr int kDecodeThreads = 128;
@@ -103,6 +146,9 @@ struct DecodeArgs {
   int Hq, Hkv, w, s, splits;
   int max_keys;      // slots one CTA stages at most (sizes its shared memory)
   float scale_log2;
+  // paged layout (kc/vc are then the page pools [n_pages, Hkv, page_size, D])
+  const int *page_table;  // [B, max_pages]
+  int page_size, max_pages, n_pages;
 };
 
 constexpr int kDecodeChunk = kDecodeMaxKeys;  // keys per chunk: one chunk per CTA
@@ -140,7 +186,11 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
 // an online softmax across chunks; with kDecodeChunk = kDecodeMaxKeys a CTA
 // has a single chunk, K first and V second, so the scores start while V is
 // still arriving.
-template <int D, int HG>
+//
+// kPaged: the cache is paged. The CTA's keys are then the positions of K(pos)
+// in order (the sinks, then pos - w + 1 .. pos), and each run of them inside
+// one page is one bulk copy; key order does not change the result.
+template <int D, int HG, bool kPaged>
 __global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const DecodeArgs a) {
   constexpr int LPK = 8;            // lanes per key row in the score phase
   constexpr int EPL = D / LPK;      // elements of a row per lane (16 or 8)
@@ -161,6 +211,7 @@ __global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const Decode
   float2 *sO = reinterpret_cast<float2 *>(                             // [kParts][HG][kPairs]
       (reinterpret_cast<uintptr_t>(sF + HG) + 15) & ~uintptr_t(15));
   __shared__ int abort_word;
+  __shared__ int missing_page;
 
   const int split = blockIdx.x;
   const int G = a.Hq / a.Hkv;
@@ -206,11 +257,48 @@ __global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const Decode
   const size_t row_base = ((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w) + k_begin;
   if (threadIdx.x == 0) {
     abort_word = 0;
+    missing_page = 0;
     for (int c = 0; c < n_chunks; ++c) {
       mbar_init(&bar_k[c], 1);
       mbar_init(&bar_v[c], 1);
     }
     fence_mbar_init();
+  }
+  if constexpr (kPaged) {
+    // keys k_begin .. k_begin + nk - 1 of the list [sinks | window] (one chunk:
+    // nk <= kDecodeMaxKeys); every page is checked before any copy is issued
+    if (threadIdx.x == 0 && nk > 0) {
+      const int ns = imin(a.s, pos + 1);              // sink positions held
+      const long long lo = imax(a.s, pos - a.w + 1);  // first window position
+      const int *tbl = a.page_table + (size_t)b * a.max_pages;
+      for (int pass = 0; pass < 2 && !missing_page; ++pass) {
+        if (pass == 1) {
+          mbar_arrive_expect_tx(&bar_k[0], (uint32_t)nk * D * 2);
+          mbar_arrive_expect_tx(&bar_v[0], (uint32_t)nk * D * 2);
+        }
+        for (int i = k_begin; i < k_begin + nk;) {
+          const long long p = i < ns ? i : lo + (i - ns);
+          const int seg_end = i < ns ? imin(k_begin + nk, ns) : k_begin + nk;
+          const long long lp = p / a.page_size;
+          const int row = (int)(p % a.page_size);
+          const int len = imin(seg_end - i, a.page_size - row);
+          const int page = lp < a.max_pages ? tbl[lp] : -1;
+          if (page < 0 || page >= a.n_pages) {
+            missing_page = 1;
+            record_error(kErrMissingPage);
+            break;
+          }
+          if (pass == 1) {
+            const size_t src = (((size_t)page * a.Hkv + kvh) * a.page_size + row) * D;
+            const uint32_t bytes = (uint32_t)len * D * 2;
+            bulk_load(sK + (size_t)(i - k_begin) * D, a.kc + src, bytes, &bar_k[0]);
+            bulk_load(sV + (size_t)(i - k_begin) * D, a.vc + src, bytes, &bar_v[0]);
+          }
+          i += len;
+        }
+      }
+    }
+  } else if (threadIdx.x == 0) {
     // every chunk's K first, then every chunk's V: the scores need K first
     for (int c = 0; c < n_chunks; ++c) {
       const int kc = imin(kDecodeChunk, nk - c * kDecodeChunk);
@@ -254,6 +342,7 @@ __global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const Decode
 #pragma unroll
   for (int h = 0; h < HG; ++h) o2[h] = make_float2(0.f, 0.f);
   __syncthreads();  // barriers initialised
+  if (kPaged && missing_page) return;  // nothing was copied
 
   for (int c = 0; c < n_chunks; ++c) {
     const int j_base = c * kDecodeChunk;

@@ -15,6 +15,7 @@ enum DeviceError : int {
   kErrNone = 0,
   kErrWaitTimeout = 1,      // a bounded mbarrier wait gave up
   kErrNegativePosition = 2, // append/decode got a position < 0
+  kErrMissingPage = 3,      // a paged append/decode met an unmapped page
 };
 
 __device__ int g_device_error;

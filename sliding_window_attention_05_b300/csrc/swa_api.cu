@@ -16,6 +16,7 @@
 #include "../../include/swa.h"
 #include "chunk.cuh"
 #include "decode.cuh"
+#include "page_pool.h"
 #include "prefill.cuh"
 #include "sm100_ptx.cuh"
 #include "swa_index.cuh"
@@ -255,33 +256,39 @@ size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
   return n * d * sizeof(float) + n * sizeof(float2);
 }
 
-template <int D, int HG>
+template <int D, int HG, bool kPaged>
 cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   const size_t smem = swa::DecodeSmem<D, HG>::bytes(a.max_keys);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(swa::swa_decode_kernel<D, HG>,
+    attr_err = cudaFuncSetAttribute(swa::swa_decode_kernel<D, HG, kPaged>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)swa::DecodeSmem<D, HG>::bytes(swa::kDecodeMaxKeys));
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(a.splits, a.Hkv * (G / HG), B);
-  cudaError_t e = launch_pdl(swa::swa_decode_kernel<D, HG>, grid, dim3(swa::kDecodeThreads),
-                             smem, stream, a);
+  cudaError_t e = launch_pdl(swa::swa_decode_kernel<D, HG, kPaged>, grid,
+                             dim3(swa::kDecodeThreads), smem, stream, a);
   if (e != cudaSuccess || a.splits == 1) return e;
   return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(B * a.Hq), dim3(D), 0, stream,
                     a.part_o, a.part_ml, a.out, a.splits);
 }
 
+template <int D, bool kPaged>
+cudaError_t launch_decode_p(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
+  switch (head_group(B, a.Hq, a.Hkv, (long long)a.w + a.s)) {
+    case 4: return launch_decode_t<D, 4, kPaged>(a, B, stream);
+    case 2: return launch_decode_t<D, 2, kPaged>(a, B, stream);
+    default: return launch_decode_t<D, 1, kPaged>(a, B, stream);
+  }
+}
+
 template <int D>
 cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
-  switch (head_group(B, a.Hq, a.Hkv, (long long)a.w + a.s)) {
-    case 4: return launch_decode_t<D, 4>(a, B, stream);
-    case 2: return launch_decode_t<D, 2>(a, B, stream);
-    default: return launch_decode_t<D, 1>(a, B, stream);
-  }
+  return a.page_table ? launch_decode_p<D, true>(a, B, stream)
+                      : launch_decode_p<D, false>(a, B, stream);
 }
 
 int check_heads(int Hq, int Hkv) {
@@ -533,7 +540,8 @@ size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {
 int decode_impl(const void *q, const void *k_new, const void *v_new, const void *kcache,
                 const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
                 int w, int s, float scale, void *workspace, size_t workspace_bytes,
-                swa_stream_t stream);
+                swa_stream_t stream, const int *page_table = nullptr, int page_size = 0,
+                int max_pages = 0, int n_pages = 0);
 
 int swa_decode(const void *q, const void *kcache, const void *vcache, const int *pos, void *out,
                int B, int Hq, int Hkv, int d, int w, int s, float scale, void *workspace,
@@ -556,7 +564,8 @@ int swa_append_decode(const void *q, const void *k_new, const void *v_new, void 
 int decode_impl(const void *q, const void *k_new, const void *v_new, const void *kcache,
                 const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
                 int w, int s, float scale, void *workspace, size_t workspace_bytes,
-                swa_stream_t stream) {
+                swa_stream_t stream, const int *page_table, int page_size, int max_pages,
+                int n_pages) {
   if (!q || !kcache || !vcache || !pos || !out) return fail(SWA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
     return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -590,6 +599,10 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
   a.splits = decode_splits(B, Hq, Hkv, w, s);
   a.max_keys = decode_max_keys(w, s, a.splits);
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.page_table = page_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.n_pages = n_pages;
   const size_t n = (size_t)B * Hq * a.splits;
   a.part_o = a.splits > 1 ? reinterpret_cast<float *>(workspace) : nullptr;
   a.part_ml = a.splits > 1 ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(workspace) +
@@ -620,6 +633,155 @@ int swa_decode_noalloc(const void *q, const void *kcache, const void *vcache, co
   }
   return swa_decode(q, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale, scratch,
                     need > 0 ? (size_t)SWA_DECODE_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
+
+// ------------------------------------------------------------ paged layout
+
+swa_page_pool *swa_page_pool_create(int n_pages) {
+  if (n_pages < 1) {
+    fail(SWA_ERR_INVALID_ARG, "n_pages must be >= 1");
+    return nullptr;
+  }
+  swa_page_pool *pool = new (std::nothrow) swa_page_pool;
+  if (!pool) {
+    fail(SWA_ERR_INVALID_ARG, "out of host memory");
+    return nullptr;
+  }
+  pool->n_pages = n_pages;
+  pool->used.assign((size_t)n_pages, 0);
+  pool->free_pages.reserve((size_t)n_pages);
+  for (int i = n_pages - 1; i >= 0; --i) pool->free_pages.push_back(i);  // hands out 0, 1, ...
+  return pool;
+}
+
+void swa_page_pool_destroy(swa_page_pool *pool) { delete pool; }
+
+int swa_page_pool_free_pages(swa_page_pool *pool) {
+  if (!pool) return -1;
+  std::lock_guard<std::mutex> lock(pool->mu);
+  return (int)pool->free_pages.size();
+}
+
+int swa_paged_reserve(swa_page_pool *pool, int *table, int max_pages, long long pos_hi, int w,
+                      int s, int page_size) {
+  if (!pool || !table) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (max_pages < 1 || pos_hi < 0 || w < 1 || s < 0 || page_size < 1)
+    return fail(SWA_ERR_INVALID_ARG, "need max_pages, w, page_size >= 1 and pos_hi, s >= 0");
+  const long long last = pos_hi / page_size;
+  if (last >= max_pages)
+    return fail(SWA_ERR_UNSUPPORTED, "position %lld is beyond the %d-page table", pos_hi,
+                max_pages);
+  const long long sink_pages = ((long long)s + page_size - 1) / page_size;
+  const long long win_lo = (pos_hi - w + 1 > 0 ? pos_hi - w + 1 : 0) / page_size;
+  const long long sink_top = sink_pages < last + 1 ? sink_pages : last + 1;  // sink pages in use
+  const long long keep_lo = win_lo > sink_pages ? win_lo : sink_pages;      // window pages
+  std::lock_guard<std::mutex> lock(pool->mu);
+  auto valid = [&](int pg) { return pg >= 0 && pg < pool->n_pages && pool->used[(size_t)pg]; };
+  // Past the sink pages, the mapped pages form one run (pages are mapped and
+  // released in position order). Find it from the top: the unmapped pages
+  // above it, then the run itself. This costs the window plus whatever the
+  // positions moved since the last call, not the whole table.
+  long long lp = last;
+  while (lp >= sink_pages && table[lp] < 0) --lp;
+  const long long run_top = lp;
+  while (lp >= sink_pages && table[lp] >= 0) {
+    if (!valid(table[lp]))
+      return fail(SWA_ERR_INVALID_ARG, "page table entry %lld was not handed out by this pool", lp);
+    --lp;
+  }
+  const long long run_bot = lp + 1;  // run = [run_bot, run_top], possibly empty
+  // leaving: the run below the window; coming: unmapped sink and window pages
+  const long long rel_lo = run_bot, rel_hi = run_top < keep_lo - 1 ? run_top : keep_lo - 1;
+  const long long n_rel = rel_hi >= rel_lo ? rel_hi - rel_lo + 1 : 0;
+  // window pages outside the run: below it (only if it starts inside the
+  // window) and above it
+  const long long a_lo = keep_lo, a_hi = run_bot - 1 < last ? run_bot - 1 : last;
+  const long long b_lo = run_top + 1 > keep_lo ? run_top + 1 : keep_lo, b_hi = last;
+  long long need = 0;
+  for (long long i = 0; i < sink_top; ++i) need += table[i] < 0;
+  for (long long i = a_lo; i <= a_hi; ++i) need += table[i] < 0;
+  for (long long i = b_lo; i <= b_hi; ++i) need += table[i] < 0;
+  if (need > (long long)pool->free_pages.size() + n_rel)
+    return fail(SWA_ERR_UNSUPPORTED, "page pool exhausted: %lld pages needed, %zu free", need,
+                pool->free_pages.size());
+  for (long long i = rel_lo; i <= rel_hi; ++i) {
+    pool->used[(size_t)table[i]] = 0;
+    pool->free_pages.push_back(table[i]);
+    table[i] = -1;
+  }
+  auto take = [&](long long i) {
+    const int pg = pool->free_pages.back();
+    pool->free_pages.pop_back();
+    pool->used[(size_t)pg] = 1;
+    table[i] = pg;
+  };
+  for (long long i = 0; i < sink_top; ++i)
+    if (table[i] < 0) take(i);
+  for (long long i = a_lo; i <= a_hi; ++i)
+    if (table[i] < 0) take(i);
+  for (long long i = b_lo; i <= b_hi; ++i)
+    if (table[i] < 0) take(i);
+  return SWA_OK;
+}
+
+int swa_paged_release(swa_page_pool *pool, int *table, int max_pages) {
+  if (!pool || !table) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (max_pages < 1) return fail(SWA_ERR_INVALID_ARG, "max_pages must be >= 1");
+  std::lock_guard<std::mutex> lock(pool->mu);
+  for (int lp = 0; lp < max_pages; ++lp) {
+    const int pg = table[lp];
+    if (pg < 0) continue;
+    if (pg >= pool->n_pages || !pool->used[(size_t)pg])
+      return fail(SWA_ERR_INVALID_ARG, "page table entry %d was not handed out by this pool", lp);
+    pool->used[(size_t)pg] = 0;
+    pool->free_pages.push_back(pg);
+    table[lp] = -1;
+  }
+  return SWA_OK;
+}
+
+int swa_paged_append(const void *k_new, const void *v_new, void *kpool, void *vpool,
+                     const int *page_table, const int *pos_start, int B, int T, int Hkv, int d,
+                     int page_size, int max_pages, int n_pages, int w, int s,
+                     swa_stream_t stream) {
+  if (!k_new || !v_new || !kpool || !vpool || !page_table || !pos_start)
+    return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kpool) || !aligned16(vpool))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || T < 1 || Hkv < 1) return fail(SWA_ERR_INVALID_ARG, "B, T and Hkv must be >= 1");
+  if (w < 1 || s < 0) return fail(SWA_ERR_INVALID_ARG, "need w >= 1 and s >= 0");
+  if (page_size < 1 || max_pages < 1 || n_pages < 1)
+    return fail(SWA_ERR_INVALID_ARG, "page_size, max_pages and n_pages must be >= 1");
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if (B > 65535) return fail(SWA_ERR_UNSUPPORTED, "B > 65535");
+  DeviceInfo dev;
+  int rc = current_device_info(&dev);
+  if (rc) return rc;
+  const int max_surv = (int)(T < (long long)s + w ? T : (long long)s + w);
+  const long long n = (long long)max_surv * Hkv * (d / 8);
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "append too large");
+  cudaError_t e = launch_pdl(
+      swa::swa_paged_append_kernel, dim3((unsigned)blocks, B), dim3(threads), 0,
+      reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const uint4 *>(k_new),
+      reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<uint4 *>(kpool),
+      reinterpret_cast<uint4 *>(vpool), page_table, pos_start, T, Hkv, d, w, s, max_surv,
+      page_size, max_pages, n_pages);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_paged_append launch");
+  return SWA_OK;
+}
+
+int swa_paged_decode(const void *q, const void *kpool, const void *vpool, const int *page_table,
+                     const int *pos, void *out, int B, int Hq, int Hkv, int d, int page_size,
+                     int max_pages, int n_pages, int w, int s, float scale, void *workspace,
+                     size_t workspace_bytes, swa_stream_t stream) {
+  if (!page_table) return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (page_size < 1 || max_pages < 1 || n_pages < 1)
+    return fail(SWA_ERR_INVALID_ARG, "page_size, max_pages and n_pages must be >= 1");
+  return decode_impl(q, nullptr, nullptr, kpool, vpool, pos, out, B, Hq, Hkv, d, w, s, scale,
+                     workspace, workspace_bytes, stream, page_table, page_size, max_pages,
+                     n_pages);
 }
 
 int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
