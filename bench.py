@@ -306,8 +306,7 @@ def run_gpu(args):
           for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    clocks_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None
+    clocks_path = args.clocks_csv
     barrier(world)
     torch.cuda.synchronize(device)
     with ClockSampler(local, clocks_path) as clk:
@@ -699,6 +698,8 @@ def main(argv=None):
     ap.add_argument("--traffic", type=float, default=PREFILL_TRAFFIC_BYTES,
                     help="DRAM bytes per prefill launch from an ncu capture of this kernel")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also write the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--ref-rows", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
