@@ -11,7 +11,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/swa.h"
 #include "chunk.cuh"
@@ -74,6 +76,23 @@ int current_device_info(DeviceInfo *info) {
 }
 
 // ------------------------------------------------------------------ launches
+
+// The dynamic shared-memory limit of a kernel is a per-device attribute:
+// raise it once per (kernel, device) that launches it.
+cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, int> raised;  // -> bytes
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = raised.find(key);
+  if (it != raised.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) raised[key] = bytes;
+  return e;
+}
 
 // Launch with programmatic stream serialisation: the kernel may begin while
 // the previous kernel on the stream finishes; it waits for that kernel
@@ -176,13 +195,8 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   const int stages = prefill_stages(D, plan, dev.max_smem_optin);
   if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
   const size_t smem = swa::PrefillSmem<D>::bytes(plan, stages, sep_stage);
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(swa::swa_prefill_kernel<D>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    dev.max_smem_optin);
-  });
+  const cudaError_t attr_err = ensure_max_dynamic_smem(
+      reinterpret_cast<const void *>(swa::swa_prefill_kernel<D>), dev.max_smem_optin);
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
 
   swa::PrefillArgs a;
@@ -260,13 +274,9 @@ template <int D, int HG, bool kPaged>
 cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
   const int G = a.Hq / a.Hkv;
   const size_t smem = swa::DecodeSmem<D, HG>::bytes(a.max_keys);
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [&] {
-    attr_err = cudaFuncSetAttribute(swa::swa_decode_kernel<D, HG, kPaged>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)swa::DecodeSmem<D, HG>::bytes(swa::kDecodeMaxKeys));
-  });
+  const cudaError_t attr_err = ensure_max_dynamic_smem(
+      reinterpret_cast<const void *>(swa::swa_decode_kernel<D, HG, kPaged>),
+      (int)swa::DecodeSmem<D, HG>::bytes(swa::kDecodeMaxKeys));
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(a.splits, a.Hkv * (G / HG), B);
   cudaError_t e = launch_pdl(swa::swa_decode_kernel<D, HG, kPaged>, grid,
