@@ -22,6 +22,9 @@ Parity status of each function (what pins it, see tests/test_oracle.py):
   decode             pinned: equals the prefill row at the same position
   ring_contents      pinned: page example (W=4, 5th token evicts the 1st), holds
                      exactly K(last), 68-slot footprint
+  prefill_backward   pinned: torch fp64 autograd of SDPA with the same boolean mask
+                     (library), w=1 closed form, keys' gradients sum to zero,
+                     Euler identity sum_j v_j.dv_j = sum_t dout_t.out_t
 """
 from __future__ import annotations
 
@@ -80,6 +83,9 @@ def _bind(lib):
     lib.oracle_prefill.restype = ctypes.c_int
     lib.oracle_prefill.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
                                    ctypes.c_double, _p, _i64, _p, _p, ctypes.c_int]
+    lib.oracle_prefill_backward.restype = ctypes.c_int
+    lib.oracle_prefill_backward.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                            _i64, ctypes.c_double, _p, _p, _p, ctypes.c_int]
     lib.oracle_decode.restype = ctypes.c_int
     lib.oracle_decode.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
                                   ctypes.c_double, _p, _p]
@@ -154,6 +160,30 @@ def prefill(q, k, v, w: int, s: int, scale: float, rows=None, nthreads: int = 0,
     if rc != 0:
         raise ValueError(f"oracle_prefill rejected its arguments (rc={rc})")
     return out, lse
+
+
+def prefill_backward(q, k, v, dout, w: int, s: int, scale: float, nthreads: int = 0, lib=None):
+    """(dq [B,L,Hq,d], dk, dv [B,L,Hkv,d]) in float64: the gradients of the
+    prefill outputs with respect to q, k, v for the upstream gradient dout
+    ([B,L,Hq,d], any float type; used in float64)."""
+    lib = lib or load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, L, Hq, d = qb.shape
+    Hkv = kb.shape[2]
+    g = dout.detach().cpu().double().numpy() if isinstance(dout, torch.Tensor) else dout
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    assert g.shape == (B, L, Hq, d), g.shape
+    dq = np.zeros((B, L, Hq, d), dtype=np.float64)
+    dk = np.zeros((B, L, Hkv, d), dtype=np.float64)
+    dv = np.zeros((B, L, Hkv, d), dtype=np.float64)
+    if nthreads <= 0:
+        nthreads = os.cpu_count() or 1
+    rc = lib.oracle_prefill_backward(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(g), B, L, Hq, Hkv, d, w,
+                                     s, float(np.float32(scale)), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_backward rejected its arguments (rc={rc})")
+    return dq, dk, dv
 
 
 def weights(q, k, w: int, s: int, scale: float, b: int, hq: int, t: int, lib=None):

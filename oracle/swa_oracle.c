@@ -180,6 +180,80 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return 0;
 }
 
+/* Backward of the prefill: the gradients of the outputs' definition above
+ * with respect to q, k and v, for an upstream gradient dout. The pages give
+ * no backward formulas (they mention SWA-aware fine-tuning only); this is the
+ * chain rule applied to that definition, term by term:
+ *   for every (b, hq, t), over j in K(t):
+ *     x_j = scale q_t . k_j,  p = softmax(x),  dp_j = dout_t . v_j,
+ *     delta = sum_j p_j dp_j,  ds_j = p_j (dp_j - delta),
+ *     dq_t  = scale sum_j ds_j k_j,
+ *     dk_j += scale ds_j q_t,  dv_j += p_j dout_t,
+ * with k_j, v_j the rows of KV head hq / (Hq / Hkv), so dk and dv sum over the
+ * query heads of a group.
+ *   q, k, v bf16 bit patterns ([B, L, Hq, d], [B, L, Hkv, d]); dout double
+ *   [B, L, Hq, d]; dq double [B, L, Hq, d]; dk, dv double [B, L, Hkv, d]
+ *   (all three written). One work item per (b, KV head) owns its dk and dv
+ *   rows and its group's dq rows. Returns 0, or -1 for an invalid argument. */
+int oracle_prefill_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const double *dout, int64_t B, int64_t L, int64_t Hq,
+                            int64_t Hkv, int64_t d, int64_t w, int64_t s, double scale,
+                            double *dq, double *dk, double *dv, int nthreads)
+{
+    if (B < 0 || L < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || w < 1 || s < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    int64_t group = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)(B * L * Hq * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * L * Hkv * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * L * Hkv * d));
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (int64_t wi = 0; wi < B * Hkv; ++wi) {
+        int64_t b = wi / Hkv, kvh = wi % Hkv;
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
+        double *p = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        for (int64_t hq = kvh * group; hq < (kvh + 1) * group; ++hq) {
+            for (int64_t t = 0; t < L; ++t) {
+                int64_t n = oracle_keyset(t, w, s, keys);
+                const uint16_t *qrow = q + ((b * L + t) * Hq + hq) * d;
+                const double *gout = dout + ((b * L + t) * Hq + hq) * d;
+                double m = -INFINITY;
+                for (int64_t i = 0; i < n; ++i) {
+                    const uint16_t *krow = k + ((b * L + keys[i]) * Hkv + kvh) * d;
+                    const uint16_t *vrow = v + ((b * L + keys[i]) * Hkv + kvh) * d;
+                    double dot = 0.0, g = 0.0;
+                    for (int64_t c = 0; c < d; ++c) {
+                        dot += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+                        g += gout[c] * bf16_to_double(vrow[c]);
+                    }
+                    p[i] = scale * dot;
+                    dp[i] = g;
+                    if (p[i] > m) m = p[i];
+                }
+                double z = 0.0;
+                for (int64_t i = 0; i < n; ++i) { p[i] = exp(p[i] - m); z += p[i]; }
+                double delta = 0.0;
+                for (int64_t i = 0; i < n; ++i) { p[i] /= z; delta += p[i] * dp[i]; }
+                double *dqrow = dq + ((b * L + t) * Hq + hq) * d;
+                for (int64_t i = 0; i < n; ++i) {
+                    const double ds = p[i] * (dp[i] - delta);
+                    const uint16_t *krow = k + ((b * L + keys[i]) * Hkv + kvh) * d;
+                    double *dkrow = dk + ((b * L + keys[i]) * Hkv + kvh) * d;
+                    double *dvrow = dv + ((b * L + keys[i]) * Hkv + kvh) * d;
+                    for (int64_t c = 0; c < d; ++c) {
+                        dqrow[c] += scale * ds * bf16_to_double(krow[c]);
+                        dkrow[c] += scale * ds * bf16_to_double(qrow[c]);
+                        dvrow[c] += p[i] * gout[c];
+                    }
+                }
+            }
+        }
+        free(keys); free(p); free(dp);
+    }
+    return 0;
+}
+
 /* Decode: one new query per head at position pos, attending over K(pos).
  * The caller passes a logical history: nh rows with positions hist_pos[i] and
  * key/value rows hist_k/hist_v [nh, Hkv, d] (bf16 bit patterns), holding at

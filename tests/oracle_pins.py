@@ -235,6 +235,66 @@ def check_footprint(lib):
     assert len(oracle.keyset(g["context"] - 1, g["w"], g["s"], lib=lib)) == g["held_tokens"]
 
 
+# ---------------------------------------------------------------- backward
+
+def _bwd_case(B=2, L=24, Hq=4, Hkv=2, d=16, seed=71):
+    q, k, v = swa_inputs.prefill_inputs(B, L, Hq, Hkv, d, seed, sink_rows=2)
+    g = torch.Generator("cpu").manual_seed(seed + 1)
+    dout = torch.randn(B, L, Hq, d, generator=g, dtype=torch.float64)
+    return q, k, v, dout
+
+
+def check_backward_vs_sdpa_autograd(lib):
+    """Gradients equal torch fp64 autograd through scaled_dot_product_attention
+    with the same boolean mask (a library routine), GQA by repeated heads."""
+    for (w, s) in ((6, 2), (24, 0), (1, 3)):
+        q, k, v, dout = _bwd_case()
+        B, L, Hq, d = q.shape
+        G = Hq // k.shape[2]
+        scale = 1.0 / math.sqrt(d)
+        qd, kd, vd = (x.double().requires_grad_(True) for x in (q, k, v))
+        mask = torch.from_numpy(oracle.swa_mask(L, w, s) & np.tril(np.ones((L, L), dtype=bool)))
+        o = F.scaled_dot_product_attention(
+            qd.permute(0, 2, 1, 3), kd.repeat_interleave(G, dim=2).permute(0, 2, 1, 3),
+            vd.repeat_interleave(G, dim=2).permute(0, 2, 1, 3), attn_mask=mask,
+            scale=float(np.float32(scale)))
+        (o.permute(0, 2, 1, 3) * dout).sum().backward()
+        dq, dk, dv = oracle.prefill_backward(q, k, v, dout, w, s, scale, lib=lib)
+        for name, got, want in (("dq", dq, qd.grad), ("dk", dk, kd.grad), ("dv", dv, vd.grad)):
+            want = want.numpy()
+            err = np.abs(got - want).max() / max(np.abs(want).max(), 1e-300)
+            assert err < 1e-10, (w, s, name, err)
+
+
+def check_backward_window_one(lib):
+    """w = 1, s = 0: out_t = v_t, so dv_t is the group's dout_t and dq = dk = 0."""
+    q, k, v, dout = _bwd_case()
+    Hkv = k.shape[2]
+    dq, dk, dv = oracle.prefill_backward(q, k, v, dout, 1, 0, 0.25, lib=lib)
+    assert not dq.any() and not dk.any()
+    want = dout.numpy().reshape(dout.shape[0], dout.shape[1], Hkv, -1, dout.shape[3]).sum(3)
+    assert np.allclose(dv, want, rtol=0, atol=1e-15)
+
+
+def check_backward_key_shift_invariance(lib):
+    """Adding one vector to every key leaves each softmax, hence every output,
+    unchanged: the key gradients of a (b, KV head) sum to zero."""
+    q, k, v, dout = _bwd_case()
+    _, dk, _ = oracle.prefill_backward(q, k, v, dout, 7, 2, 0.25, lib=lib)
+    tot = dk.sum(axis=1)                       # over positions -> [B, Hkv, d]
+    assert np.abs(tot).max() <= 1e-12 * max(np.abs(dk).max(), 1.0)
+
+
+def check_backward_euler_identity(lib):
+    """Every output is linear in V: sum_j v_j . dv_j = sum_t dout_t . out_t."""
+    q, k, v, dout = _bwd_case()
+    _, _, dv = oracle.prefill_backward(q, k, v, dout, 5, 3, 0.25, lib=lib)
+    out, _ = oracle.prefill(q, k, v, 5, 3, 0.25, lib=lib)
+    lhs = float((v.double().numpy() * dv).sum())
+    rhs = float((dout.numpy() * out).sum())
+    assert abs(lhs - rhs) <= 1e-10 * max(abs(rhs), 1.0), (lhs, rhs)
+
+
 ALL_CHECKS = [
     check_keymask_vs_pseudocode,
     check_counts_closed_form,
@@ -253,4 +313,8 @@ ALL_CHECKS = [
     check_ring_page_example,
     check_ring_holds_keyset,
     check_footprint,
+    check_backward_vs_sdpa_autograd,
+    check_backward_window_one,
+    check_backward_key_shift_invariance,
+    check_backward_euler_identity,
 ]

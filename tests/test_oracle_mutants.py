@@ -20,6 +20,11 @@ MUTANTS = {
     "not_normalised": ("out[c] = acc / z;", "out[c] = acc / (z + 1e-3);"),
     "ring_wraps_wrong": ("if (ptr == w) ptr = 0;", "if (ptr == w) ptr = 1 % w;"),
     "ring_sinks_evicted": ("if (p < s) {", "if (p < 0) {"),
+    "bwd_delta_dropped": ("delta += p[i] * dp[i];", "delta += 0.0 * dp[i];"),
+    "bwd_dk_sign": ("dkrow[c] += scale * ds", "dkrow[c] -= scale * ds"),
+    "bwd_dq_scale_dropped": ("dqrow[c] += scale * ds", "dqrow[c] += ds"),
+    "bwd_dv_unweighted": ("dvrow[c] += p[i] * gout[c];", "dvrow[c] += gout[c] / n;"),
+    "bwd_group_first_head_only": ("hq < (kvh + 1) * group; ++hq)", "hq < kvh * group + 1; ++hq)"),
 }
 
 
