@@ -18,7 +18,8 @@ Parity status of each function (what pins it, see tests/test_oracle.py):
   keyset / keymask   pinned: explicit boolean mask, closed-form counts, w>=L, s=0
   prefill            pinned: torch fp64 SDPA with the same boolean mask (library),
                      w=1 identity, q=0 mean, constant-V, GQA == repeated MHA
-  weights            pinned: rows sum to one, agree with SDPA probabilities
+  weights            pinned: rows sum to one; equal torch fp64 softmax (library) of
+                     the scaled scores over the same boolean mask, GQA group of 3
   decode             pinned: equals the prefill row at the same position
   ring_contents      pinned: page example (W=4, 5th token evicts the 1st), holds
                      exactly K(last), 68-slot footprint

@@ -136,6 +136,33 @@ def _bf16_cuda(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _expect_shape(t: torch.Tensor | None, shape, name: str):
+    """Raise ValueError unless t (if given) has exactly this shape."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _ndim(t: torch.Tensor, n: int, name: str):
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+
+
+def _check_cache(kcache: torch.Tensor, vcache: torch.Tensor, B: int, d: int, w: int, s: int):
+    """The ring cache of these sizes: K and V [B, Hkv, s + w, d] (the library
+    derives its strides from w and s alone, so any other shape would be read or
+    written out of bounds)."""
+    _ndim(kcache, 4, "kcache")
+    want = (B, kcache.shape[1], int(s) + int(w), d)
+    _expect_shape(kcache, want, "kcache ([B, Hkv, s + w, d])")
+    _expect_shape(vcache, want, "vcache ([B, Hkv, s + w, d])")
+
+
+def _check_pos(pos: torch.Tensor, B: int, name: str = "pos"):
+    _expect_shape(pos, (B,), name)
+    if pos.dtype != torch.int32 or not pos.is_cuda:
+        raise TypeError(f"{name} must be a CUDA int32 tensor")
+
+
 def _default_scale(d: int, scale):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
@@ -150,6 +177,12 @@ def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: in
     host-buffer path: they are copied to the current device, the kernel runs,
     and the result is copied back to a (pinned) host tensor before returning.
     """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _ndim(t, 4, n)
+    B, L, Hq, d = q.shape
+    if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    _expect_shape(out, q.shape, "out")
     if not q.is_cuda:
         dev = torch.device("cuda", torch.cuda.current_device())
         qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
@@ -160,9 +193,6 @@ def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: in
         return host
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _bf16_cuda(t, n)
-    B, L, Hq, d = q.shape
-    if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
-        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     Hkv = k.shape[2]
     if out is None:
         out = torch.empty_like(q)
@@ -196,13 +226,14 @@ def swa_cache_bytes(B: int, Hkv: int, d: int, w: int, s: int) -> int:
 def swa_cache_append(k_new: torch.Tensor, v_new: torch.Tensor, kcache: torch.Tensor,
                      vcache: torch.Tensor, pos_start: torch.Tensor, w: int, s: int, stream=None):
     """Append tokens k_new/v_new [B,T,Hkv,d] at positions pos_start[b] + i."""
-    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"), (vcache, "vcache")):
-        _bf16_cuda(t, n)
-    if pos_start.dtype != torch.int32 or not pos_start.is_cuda:
-        raise TypeError("pos_start must be a CUDA int32 tensor")
+    _ndim(k_new, 4, "k_new")
     B, T, Hkv, d = k_new.shape
+    _expect_shape(v_new, k_new.shape, "v_new")
     if kcache.shape != (B, Hkv, s + w, d) or vcache.shape != kcache.shape:
         raise ValueError(f"cache must be [B, Hkv, s + w, d] = {(B, Hkv, s + w, d)}")
+    _check_pos(pos_start, B, "pos_start")
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"), (vcache, "vcache")):
+        _bf16_cuda(t, n)
     _check(_lib.swa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
                                  _ptr(pos_start), B, T, Hkv, d, int(w), int(s), _stream(stream)),
            "swa_cache_append")
@@ -216,11 +247,13 @@ def swa_decode(q: torch.Tensor, kcache: torch.Tensor, vcache: torch.Tensor, pos:
                w: int, s: int, scale: float | None = None, out: torch.Tensor | None = None,
                workspace: torch.Tensor | None = None, stream=None):
     """One decode step: q [B,Hq,d] over the ring cache holding position pos[b]."""
+    _ndim(q, 3, "q")
+    B, Hq, d = q.shape
+    _check_cache(kcache, vcache, B, d, w, s)
+    _expect_shape(out, q.shape, "out")
+    _check_pos(pos, B)
     for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
         _bf16_cuda(t, n)
-    if pos.dtype != torch.int32 or not pos.is_cuda:
-        raise TypeError("pos must be a CUDA int32 tensor")
-    B, Hq, d = q.shape
     Hkv = kcache.shape[1]
     if out is None:
         out = torch.empty_like(q)
@@ -240,15 +273,17 @@ def swa_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       workspace: torch.Tensor | None = None, stream=None):
     """Append the token k_new/v_new [B,Hkv,d] at position pos[b], then decode
     q [B,Hq,d] over the cache (one launch)."""
-    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
-                 (vcache, "vcache")):
-        _bf16_cuda(t, n)
-    if pos.dtype != torch.int32 or not pos.is_cuda:
-        raise TypeError("pos must be a CUDA int32 tensor")
+    _ndim(q, 3, "q")
     B, Hq, d = q.shape
+    _check_cache(kcache, vcache, B, d, w, s)
     Hkv = kcache.shape[1]
     if k_new.shape != (B, Hkv, d) or v_new.shape != k_new.shape:
         raise ValueError(f"k_new/v_new must be [B, Hkv, d] = {(B, Hkv, d)}")
+    _expect_shape(out, q.shape, "out")
+    _check_pos(pos, B)
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
+                 (vcache, "vcache")):
+        _bf16_cuda(t, n)
     if out is None:
         out = torch.empty_like(q)
     need = swa_decode_workspace_size(B, Hq, Hkv, d, w, s)
@@ -273,13 +308,16 @@ def swa_prefill_chunk(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       workspace: torch.Tensor | None = None, stream=None):
     """Prefill the chunk q [B,T,Hq,d], k_new/v_new [B,T,Hkv,d] at positions
     pos0 .. pos0+T-1 against the ring cache, then append it; returns out [B,T,Hq,d]."""
-    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
-                 (vcache, "vcache")):
-        _bf16_cuda(t, n)
+    _ndim(q, 4, "q")
     B, T, Hq, d = q.shape
+    _check_cache(kcache, vcache, B, d, w, s)
     Hkv = kcache.shape[1]
     if k_new.shape != (B, T, Hkv, d) or v_new.shape != k_new.shape:
         raise ValueError(f"k_new/v_new must be [B, T, Hkv, d] = {(B, T, Hkv, d)}")
+    _expect_shape(out, q.shape, "out")
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (kcache, "kcache"),
+                 (vcache, "vcache")):
+        _bf16_cuda(t, n)
     if out is None:
         out = torch.empty_like(q)
     need = swa_prefill_chunk_workspace_size(B, T, Hq, Hkv, d, w, s, pos0)

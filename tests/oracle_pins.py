@@ -178,6 +178,30 @@ def check_weights_sum_to_one(lib):
         assert np.all(wts > 0)
 
 
+def check_weights_vs_torch_softmax(lib):
+    """Each row's weights equal torch's fp64 softmax (a library routine) of the
+    scaled scores q_t . k_j over the page's boolean mask row (clamped to
+    causal), with the query head reading KV head hq // (Hq / Hkv). The
+    configuration has a group of 3 query heads per KV head (so hq // G and
+    hq % Hkv differ for most heads) and a scale far from 1."""
+    B, L, Hq, Hkv, d, w, s, scale = 2, 33, 6, 2, 16, 5, 3, 0.37
+    q, k, _ = swa_inputs.prefill_inputs(B, L, Hq, Hkv, d, 83, sink_rows=3)
+    G = Hq // Hkv
+    kd = k.double().repeat_interleave(G, dim=2)          # [B, L, Hq, d]: head hq reads hq // G
+    mask = torch.from_numpy(oracle.swa_mask(L, w, s) & np.tril(np.ones((L, L), dtype=bool)))
+    sc = float(np.float32(scale))
+    for b in range(B):
+        for hq in range(Hq):
+            x = (q.double()[b, :, hq, :] @ kd[b, :, hq, :].T) * sc       # [L, L]
+            x = x.masked_fill(~mask, -math.inf)
+            p = torch.softmax(x, dim=1).numpy()
+            for t in range(L):
+                want = p[t][mask[t].numpy()]
+                got = oracle.weights(q, k, w, s, scale, b, hq, t, lib=lib)
+                assert got.shape == want.shape, (b, hq, t)
+                assert np.max(np.abs(got - want)) < 1e-13, (b, hq, t)
+
+
 def check_lse_vs_logsumexp(lib):
     q, k, v = swa_inputs.prefill_inputs(1, 30, 2, 2, 16, 91, sink_rows=2)
     w, s, scale = 7, 2, 0.25
@@ -308,6 +332,7 @@ ALL_CHECKS = [
     check_constant_values,
     check_gqa_equals_repeated_mha,
     check_weights_sum_to_one,
+    check_weights_vs_torch_softmax,
     check_lse_vs_logsumexp,
     check_decode_equals_prefill_row,
     check_ring_page_example,

@@ -27,9 +27,17 @@ def compare(gpu_out: torch.Tensor, ref: np.ndarray, what: str = "",
     return ma, rl
 
 
-def sample_rows(L: int, w: int, s: int, n_random: int, seed: int) -> np.ndarray:
-    """All rows t < w + s + 128, the last 128 rows, and n_random random rows."""
-    head = np.arange(min(L, w + s + 128))
+def sample_rows(L: int, w: int, s: int, n_random: int, seed: int,
+                head_cap: int | None = None) -> np.ndarray:
+    """All rows t < w + s + 128 (the rows whose window still reaches the first
+    keys, including the switch from a merged sink range to a separate sink
+    tile near t = w + s), the last 128 rows, and n_random random rows.
+    head_cap bounds the first part for full-causal layers (w >= L), where every
+    row reaches the first keys."""
+    n_head = min(L, w + s + 128)
+    if head_cap is not None:
+        n_head = min(n_head, head_cap)
+    head = np.arange(n_head)
     tail = np.arange(max(0, L - 128), L)
     rng = np.random.default_rng(seed)
     mid = rng.integers(0, L, size=n_random)

@@ -7,7 +7,7 @@ import torch
 import oracle
 import sliding_window_attention_05_b300 as swa
 import swa_inputs
-from parity import compare, prefill_case, scale_for
+from parity import compare, prefill_case, sample_rows, scale_for
 
 pytestmark = pytest.mark.gpu
 
@@ -180,9 +180,9 @@ def test_hybrid_stack_prefill_then_decode():
             dec[i] = [x.clone() for x in o]
     torch.cuda.synchronize()
     for layer, ((w, s), (q, k, v, qs, ks, vs)) in enumerate(zip(windows, host)):
-        rng = np.random.default_rng(layer)
-        rows = np.unique(np.concatenate([np.arange(64), np.arange(L - 16, L),
-                                         rng.integers(0, L, 16)]))
+        # SWA layers: every row t < w + s + 128; full layers: the first 512;
+        # both: the last 128 rows and 512 random ones
+        rows = sample_rows(L, w, s, 512, seed=layer, head_cap=512 if w >= L else None)
         ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=rows)
         compare(outs[layer][:, torch.from_numpy(rows).cuda()].cpu(), ref, f"layer {layer} prefill")
         hist_k = torch.cat([k[0], ks[:, 0, 0]], 0)

@@ -99,7 +99,7 @@ def test_long_prefill_window_sweep_sampled(w):
     q, k, v = prefill_case(B, L, Hq, Hkv, d, 1004 + w, sink_rows=4)
     sc = scale_for(d)
     out = _run(q, k, v, w, s, sc)
-    rows = sample_rows(L, w, s, 1024, seed=w)
+    rows = sample_rows(L, w, s, 4096, seed=w)
     ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=rows)
     compare(out[:, torch.from_numpy(rows).cuda()].cpu(), ref, f"long w={w}")
 
@@ -112,8 +112,9 @@ def test_hybrid_layer_prefill_sampled(w, s):
     q, k, v = prefill_case(B, L, Hq, Hkv, d, 1500 + s)
     sc = scale_for(d)
     out = _run(q, k, v, w, s, sc)
-    n_random = 512 if s else 96
-    rows = sample_rows(L, min(w, 256), s, n_random, seed=7)
+    # SWA layer: every row t < w + s + 128 = 2276; full layer: the first 4096
+    # rows (each reaches position 0); both: the last 128 and 4096 random rows
+    rows = sample_rows(L, w, s, 4096, seed=7, head_cap=4096)
     ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=rows)
     compare(out[:, torch.from_numpy(rows).cuda()].cpu(), ref, f"hybrid w={w} s={s}")
 

@@ -24,6 +24,9 @@ MUTANTS = {
     "bwd_dk_sign": ("dkrow[c] += scale * ds", "dkrow[c] -= scale * ds"),
     "bwd_dq_scale_dropped": ("dqrow[c] += scale * ds", "dqrow[c] += ds"),
     "bwd_dv_unweighted": ("dvrow[c] += p[i] * gout[c];", "dvrow[c] += gout[c] / n;"),
+    "weights_scale_dropped": ("weights[i] = scale * dot;", "weights[i] = dot;"),
+    "weights_gqa_interleaved": ("int64_t group = Hq / Hkv, kvh = hq / group;",
+                                "int64_t group = Hq / Hkv, kvh = hq % Hkv;"),
     "bwd_group_first_head_only": ("hq < (kvh + 1) * group; ++hq)", "hq < kvh * group + 1; ++hq)"),
 }
 

@@ -8,8 +8,9 @@ swa_decode_noalloc keeps the split-KV partial results in a fixed scratch array
 compiled into libswa.so instead of a caller workspace.
 
 These tests call it through the C ABI and check its output against swa_decode
-(the entry point that takes a workspace), on two calls in a row, so that the
-scratch left over from the first call cannot leak into the second.
+(the entry point that takes a workspace) and against the fp64 oracle, on two
+calls in a row, so that the scratch left over from the first call cannot leak
+into the second.
 This file is collected last on purpose: a run that stops at the first failure
 has already run every other test.
 """
@@ -19,9 +20,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import sliding_window_attention_05_b300 as swa
 import swa_inputs
-from parity import MAX_ABS, REL_L2
+from parity import MAX_ABS, REL_L2, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +74,10 @@ def test_noalloc_decode_matches_workspace_decode(B, Hq, Hkv, d, w, s, pos, split
         assert _noalloc(q, cache.k, cache.v, posd, got, w, s, scale) == swa.SWA_OK, swa.swa_last_error()
         torch.cuda.synchronize()
         _close(got, ref, f"call {call}")
+        keys = oracle.keyset(pos, w, s)
+        want = np.stack([oracle.decode(q[b].cpu(), keys, k[b, keys], v[b, keys], pos, w, s,
+                                       scale)[0] for b in range(B)])
+        compare(got.cpu(), want, f"call {call} vs oracle")
     assert swa.swa_device_error(clear=True) == 0
 
 
