@@ -2,19 +2,25 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one pass of the whole hot path over one batch of the Llama-3.1-8B
-shaped single-layer workload (B=1, L=4096, Hq=32, Hkv=8, d=128, SWA(w=128,
-s=4), bf16, q/k/v ~ N(0,1) with the four sink keys scaled x4):
+One step = one pass of the whole hot path over one batch of the long-prefill
+workload with the widest window of the sweep (B=2, L=32768, Hq=32, Hkv=8,
+d=128, SWA(w=512, s=4), bf16, q/k/v ~ N(0,1) with the four sink keys scaled
+x4; the inputs, 1.34 GB, exceed the 126 MB L2):
     swa_prefill  ->  swa_cache_append (prompt survivors)
                  ->  swa_append_decode (append one new token, decode at pos = L)
 Metric: in-band TFLOP/s = 4 * B * Hq * d * (sum over the step's query rows of
-|K(t)|) / step time. The decode half of the metric (KV GB/s at batch 64, 68-slot
-cache, SWA(64, 4)) is measured in the same run and reported under "decode".
+|K(t)|) / step time.
 
-Steps rotate over input sets whose total exceeds the 126 MB L2, each set
-replayed as one CUDA graph of the step. Timing uses CUDA events on the
-launching stream. Under torchrun each rank runs an independent replica on its
-own GPU (no data-path collective); the time is the max over ranks.
+Besides the K timed steps, each measured kernel is timed over its own fixed
+loop of at least one second of device time (CUDA graph replays on the
+launching stream), so its per-launch figure does not depend on K:
+  roofline     the prefill kernel of the step (tensor-bound at this window)
+  llama_layer  the Llama-3.1-8B shaped layer prefill (B=1, L=4096, SWA(128,4);
+               HBM-bound; rotating input sets larger than L2)
+  decode       batch-64 decode, SWA(64,4), 68-slot ring cache (HBM-bound;
+               rotating caches larger than 4x L2)
+Under torchrun each rank runs an independent replica on its own GPU (no
+data-path collective); the time is the max over ranks.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
 on a bounded sample of the same workload.
@@ -22,9 +28,11 @@ on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import time
@@ -38,16 +46,15 @@ if ROOT not in sys.path:
 
 import swa_inputs  # noqa: E402
 
-WORKLOAD = dict(name="llama3.1-8b-layer-prefill+decode SWA(128,4)", B=1, L=4096, Hq=32, Hkv=8,
-                d=128, w=128, s=4, sink_rows=4, seed=1002)
+WORKLOAD = dict(name="long prefill SWA(512,4) B=2 L=32768 + append + decode", B=2, L=32768,
+                Hq=32, Hkv=8, d=128, w=512, s=4, sink_rows=4, seed=1004)
+LLAMA = dict(name="llama3.1-8b-layer prefill SWA(128,4)", B=1, L=4096, Hq=32, Hkv=8,
+             d=128, w=128, s=4, sink_rows=4, seed=1002)
 DECODE = dict(name="decode SWA(64,4) batch 64, 68-slot ring cache", B=64, Hq=32, Hkv=8, d=128,
               w=64, s=4, pos=262143)
 L2_BYTES = 126 * 1024 * 1024
-# DRAM bytes (read + write) of one launch of the prefill kernel on WORKLOAD,
-# from an ncu capture of the current kernel (dram__bytes_read.sum 50.43 MB +
-# dram__bytes_write.sum 2.05 MB). It describes that kernel only: it goes back
-# to None whenever the kernel changes, until a new capture is taken.
-PREFILL_TRAFFIC_BYTES = 52.48e6
+KERNEL_SOURCES = ("prefill.cuh", "swa_index.cuh", "sm100_ptx.cuh")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "swa_prefill_b2_L32768_w512_s4.md")
 
 
 def pairs_per_head(L: int, w: int, s: int) -> int:
@@ -60,6 +67,10 @@ def keys_of_row(t: int, w: int, s: int) -> int:
     return min(t + 1, w) + min(s, max(0, t - w + 1))
 
 
+def prefill_flops(cfg) -> float:
+    return 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * pairs_per_head(cfg["L"], cfg["w"], cfg["s"])
+
+
 def step_flops(cfg) -> float:
     rows = pairs_per_head(cfg["L"], cfg["w"], cfg["s"]) + keys_of_row(cfg["L"], cfg["w"], cfg["s"])
     return 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * rows
@@ -68,6 +79,31 @@ def step_flops(cfg) -> float:
 def prefill_bytes(cfg) -> int:
     """Algorithmic bytes of one prefill launch: Q, K, V read once, O written once."""
     return cfg["B"] * cfg["L"] * (2 * cfg["Hq"] + 2 * cfg["Hkv"]) * cfg["d"] * 2
+
+
+def kernel_source_digest() -> str:
+    """sha256 (first 16 hex digits) of the prefill kernel's source files."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sliding_window_attention_05_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the step's prefill kernel from the committed ncu
+    summary, or None when the kernel's sources changed since that capture."""
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None, "no capture"
+    with open(TRAFFIC_PROFILE) as f:
+        text = f.read()
+    m = re.search(r"traffic_record: dram_bytes_per_launch=(\d+) source_sha=([0-9a-f]+)", text)
+    if not m:
+        return None, "no traffic record"
+    if m.group(2) != kernel_source_digest():
+        return None, f"kernel changed since the capture (sources {kernel_source_digest()}, " \
+                     f"capture {m.group(2)})"
+    return int(m.group(1)), os.path.relpath(TRAFFIC_PROFILE, ROOT)
 
 
 def load_peaks():
@@ -230,9 +266,34 @@ def launches_per_step(swa, cfg) -> int:
     return 1 + 1 + (2 if splits_ws else 1)
 
 
-def bench_decode(swa, device, stream, iters=64, warmup=8, pos=None):
+def replay_for(graph, stream, min_seconds: float, launches_per_replay: int):
+    """Replay `graph` on `stream` for at least min_seconds of device time (the
+    replay count is fixed from a short calibration first); returns
+    (ms per launch, replays)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        e0.record(stream)
+        for _ in range(5):
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        per = e0.elapsed_time(e1) / 5
+        n = max(5, int(math.ceil(min_seconds * 1e3 / max(per, 1e-3))))
+        e0.record(stream)
+        for _ in range(n):
+            graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / (n * launches_per_replay), n
+
+
+def bench_decode(swa, device, stream, min_seconds=1.0, pos=None):
     """Kernel-only decode at batch 64 over a rotating pool of distinct caches
-    (> 4x L2), replayed as one CUDA graph of `ncache` decode launches."""
+    (> 4x L2), captured as one CUDA graph of `ncache` decode launches and
+    replayed for at least min_seconds."""
     c = dict(DECODE)
     if pos is not None:
         c["pos"] = pos
@@ -254,21 +315,40 @@ def bench_decode(swa, device, stream, iters=64, warmup=8, pos=None):
         with torch.cuda.graph(graph, stream=stream):
             for kc, vc in caches:
                 swa.swa_decode(q, kc, vc, pos, w, s, out=out)
-        for _ in range(warmup):
-            graph.replay()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(iters):
-            graph.replay()
-        e1.record(stream)
-        e1.synchronize()
-    ms_per_launch = e0.elapsed_time(e1) / (iters * ncache)
+    ms_per_launch, reps = replay_for(graph, stream, min_seconds, ncache)
     kv_bytes = B * Hkv * min(c["pos"] + 1, s + w) * d * 2 * 2  # slots actually read
     gbs = kv_bytes / (ms_per_launch * 1e-3) / 1e9
     return dict(kv_bytes_per_launch=kv_bytes, us_per_launch=ms_per_launch * 1e3, gbs=gbs,
-                caches=ncache, pool_bytes=ncache * kv_bytes)
+                caches=ncache, pool_bytes=ncache * kv_bytes, launches=reps * ncache)
+
+
+def bench_llama_layer(swa, device, stream, peaks, min_seconds=1.0):
+    """The Llama-3.1-8B shaped layer prefill (B=1, L=4096, SWA(128, 4)) over
+    rotating input sets larger than L2: one CUDA graph that runs the prefill
+    once on each set, replayed for at least min_seconds."""
+    cfg = LLAMA
+    n_sets = max(2, int(math.ceil(2.5 * L2_BYTES / prefill_bytes(cfg))))
+    sets = make_step_inputs(cfg, n_sets, device)
+    steps = [GpuStep(swa, cfg, h, device) for h in sets]
+    with torch.cuda.stream(stream):
+        for st in steps:
+            st.prefill()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for st in steps:
+                st.prefill()
+    ms, reps = replay_for(graph, stream, min_seconds, n_sets)
+    by = prefill_bytes(cfg)
+    gbs = by / (ms * 1e-3) / 1e9
+    return {"workload": cfg["name"], "B": cfg["B"], "L": cfg["L"], "w": cfg["w"], "s": cfg["s"],
+            "kernel": "swa_prefill_kernel<128>", "bound": "hbm",
+            "us_per_launch": round(ms * 1e3, 2), "achieved": round(gbs, 1), "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes": by,
+            "tflops": round(prefill_flops(cfg) / (ms * 1e-3) / 1e12, 2),
+            "launches": reps * n_sets,
+            "l2": f"rotating {n_sets} input sets of {by / 1e6:.1f} MB (> 126 MB L2)"}
 
 
 def run_gpu(args):
@@ -284,19 +364,15 @@ def run_gpu(args):
     cfg = WORKLOAD
     peaks = load_peaks()
 
-    set_bytes = prefill_bytes(cfg)
-    n_sets = max(2, int(math.ceil(2.5 * L2_BYTES / set_bytes)))
-    host_sets = make_step_inputs(cfg, n_sets, device, seed_offset=1000 * rank)
-    steps = [GpuStep(swa, cfg, h, device) for h in host_sets]
+    # one input set: 1.34 GB of q, k, v, far larger than the 126 MB L2
+    host = make_step_inputs(cfg, 1, device, seed_offset=1000 * rank)[0]
+    st = GpuStep(swa, cfg, host, device)
     with torch.cuda.stream(stream):
-        for st in steps:           # eager warm-up (first-call setup happens here)
-            st.prefill()
-            st.rest()
+        st.prefill()               # eager warm-up (first-call setup happens here)
+        st.rest()
         stream.synchronize()
-        for st in steps:
-            st.capture(stream)
-        for i in range(args.warmup):
-            st = steps[i % n_sets]
+        st.capture(stream)
+        for _ in range(args.warmup):
             st.graph_prefill.replay()
             st.graph_rest.replay()
         stream.synchronize()
@@ -306,14 +382,12 @@ def run_gpu(args):
           for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    clocks_path = args.clocks_csv
     barrier(world)
     torch.cuda.synchronize(device)
-    with ClockSampler(local, clocks_path) as clk:
+    with ClockSampler(local, args.clocks_csv) as clk:
         with torch.cuda.stream(stream):
             start.record(stream)
             for i in range(K):
-                st = steps[i % n_sets]
                 ev[i][0].record(stream)
                 st.graph_prefill.replay()
                 ev[i][1].record(stream)
@@ -322,27 +396,38 @@ def run_gpu(args):
         torch.cuda.synchronize(device)
     barrier(world)
     total_ms = start.elapsed_time(end)
-    prefill_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    prefill_ms_steps = sum(a.elapsed_time(b) for a, b in ev) / K
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
     value = step_flops(cfg) * world / (ms_per_step * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (prefill): HBM-bound at this window
-    achieved = prefill_bytes(cfg) / (prefill_ms * 1e-3) / 1e9
-    roofline = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
-                    frac=round(achieved / peaks["hbm_gbs"], 4), traffic=args.traffic,
-                    kernel="swa_prefill_kernel<128>", us_per_launch=round(prefill_ms * 1e3, 2),
-                    peak_source=peaks["source"],
-                    tensor_tflops=round(4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] *
-                                        pairs_per_head(cfg["L"], cfg["w"], cfg["s"]) /
-                                        (prefill_ms * 1e-3) / 1e12, 2))
-
-    dec = bench_decode(swa, device, stream) if (rank == 0 and not args.skip_decode) else None
-    e2e = None if args.skip_e2e else run_e2e(swa, cfg, host_sets[0], device, stream,
-                                               max(3, min(K, 20)), world)
-
+    # the same step through the public API with host buffers (every rank)
+    e2e = None if args.skip_e2e else run_e2e(swa, cfg, host, device, stream,
+                                             max(3, min(K, 10)), world)
     result = None
     if rank == 0:
+        # the prefill kernel alone, over a fixed loop of >= min_seconds
+        with ClockSampler(local) as clk_loop:
+            pre_ms, pre_reps = replay_for(st.graph_prefill, stream, args.loop_seconds, 1)
+        tf = prefill_flops(cfg) / (pre_ms * 1e-3) / 1e12
+        traffic, traffic_src = recorded_traffic()
+        roofline = dict(
+            bound="tensor", achieved=round(tf, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+            frac=round(tf / peaks["bf16_tflops"], 4), traffic=traffic,
+            kernel="swa_prefill_kernel<128>", us_per_launch=round(pre_ms * 1e3, 2),
+            launches_timed=pre_reps, peak_source=peaks["source"] + " (burst)",
+            peak_sustained=peaks["bf16_tflops_sustained"],
+            frac_sustained=(round(tf / peaks["bf16_tflops_sustained"], 4)
+                            if peaks["bf16_tflops_sustained"] else None),
+            inband_flop_per_launch=prefill_flops(cfg),
+            algorithmic_bytes=prefill_bytes(cfg),
+            hbm_gbs=round(prefill_bytes(cfg) / (pre_ms * 1e-3) / 1e9, 1),
+            traffic_source=traffic_src, kernel_sources_sha=kernel_source_digest(),
+            us_per_launch_in_steps=round(prefill_ms_steps * 1e3, 2),
+            clocks=clk_loop.summary())
+        llama = None if args.skip_llama else bench_llama_layer(swa, device, stream, peaks,
+                                                               args.loop_seconds)
+        dec = None if args.skip_decode else bench_decode(swa, device, stream, args.loop_seconds)
         result = {
             "metric": "SWA(w,s) prefill in-band TFLOP/s & decode KV GB/s, % of B300 roofline",
             "value": round(value, 3),
@@ -361,21 +446,22 @@ def run_gpu(args):
                        "global_batch": cfg["B"] * world, "seq_len": cfg["L"],
                        "parallelism": f"replicas x{world}",
                        "step": "prefill + append(prompt) + append_decode(pos=L)",
-                       "l2": f"rotating {n_sets} input sets of {set_bytes / 1e6:.1f} MB "
-                             f"(> 126 MB L2), CUDA graph per set"},
+                       "l2": f"inputs larger than L2 ({prefill_bytes(cfg) / 1e9:.2f} GB of "
+                             f"q, k, v, out per step); CUDA graph per step half"},
             "roofline": roofline,
+            "llama_layer": llama,
             "decode": None if dec is None else dict(
                 workload=DECODE["name"], value=round(dec["gbs"], 1), unit="GB/s",
                 bound="hbm", peak=peaks["hbm_gbs"], frac=round(dec["gbs"] / peaks["hbm_gbs"], 4),
                 us_per_launch=round(dec["us_per_launch"], 3),
-                kv_bytes_per_launch=dec["kv_bytes_per_launch"],
+                kv_bytes_per_launch=dec["kv_bytes_per_launch"], launches_timed=dec["launches"],
                 l2=f"{dec['caches']} distinct caches, {dec['pool_bytes'] / 1e6:.0f} MB"),
             "e2e": e2e,
             "gpu_launches": launches_per_step(swa, cfg) * K,
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(cfg, host_sets[0], budget_s=args.cpu_seconds)
+            result["cpu_baseline"] = cpu_baseline(cfg, host, budget_s=args.cpu_seconds)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -622,36 +708,40 @@ def run_e2e(swa, cfg, host, device, stream, K, world):
 
 # ------------------------------------------------------------------ CPU oracle arm
 
+def _oracle_rows_timed(oracle, cfg, host, rows, nthreads):
+    sc = 1.0 / math.sqrt(cfg["d"])
+    t0 = time.perf_counter()
+    oracle.prefill(host["q"], host["k"], host["v"], cfg["w"], cfg["s"], sc, rows=rows,
+                   nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    fl = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * sum(keys_of_row(int(t), cfg["w"], cfg["s"])
+                                                     for t in rows)
+    return dt, fl
+
+
 def cpu_baseline(cfg, host, budget_s: float = 15.0):
-    """The fp64 oracle as it stands, on this host's cores: every query row of
-    every head of the workload, repeated until about budget_s seconds of CPU
-    work have run (all cores, OpenMP over rows); plus a one-thread figure over
-    a bounded sample of rows. Throughput in in-band TFLOP/s."""
+    """The fp64 oracle as it stands, on this host's cores (all threads, OpenMP
+    over rows): evenly spaced query rows of the step's prefill (every head and
+    batch), as many as fit in about budget_s seconds, after a short calibration;
+    plus a one-thread figure over a tenth of the budget. In-band TFLOP/s."""
     import oracle
     cores = os.cpu_count() or 1
-    L, w, s = cfg["L"], cfg["w"], cfg["s"]
-    sc = 1.0 / math.sqrt(cfg["d"])
-    rows = np.arange(L, dtype=np.int64)
-    flops_all = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * pairs_per_head(L, w, s)
-    reps, dt = 0, 0.0
-    while reps < 1 or (dt < budget_s and dt / reps * (reps + 1) <= 2 * budget_s):
-        t0 = time.perf_counter()
-        oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=rows, nthreads=cores)
-        dt += time.perf_counter() - t0
-        reps += 1
-    # one thread, on an evenly spaced sample of rows (about a tenth of the budget)
-    n1 = max(16, min(L, int(L * (budget_s / 10) / max(dt / reps * cores, 1e-3))))
-    rows1 = np.linspace(0, L - 1, n1).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=rows1, nthreads=1)
-    dt1 = time.perf_counter() - t0
-    fl1 = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * sum(keys_of_row(int(t), w, s) for t in rows1)
-    return {"value": round(flops_all * reps / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+    L = cfg["L"]
+    probe = np.linspace(0, L - 1, 64).astype(np.int64)
+    dt, _ = _oracle_rows_timed(oracle, cfg, host, probe, cores)
+    n = int(min(L, max(64, 64 * budget_s / max(dt, 1e-3))))
+    rows = np.unique(np.linspace(0, L - 1, n).astype(np.int64))
+    dt, fl = _oracle_rows_timed(oracle, cfg, host, rows, cores)
+    n1 = int(min(L, max(8, len(rows) * (budget_s / 10) / max(dt * cores, 1e-3))))
+    rows1 = np.unique(np.linspace(0, L - 1, n1).astype(np.int64))
+    dt1, fl1 = _oracle_rows_timed(oracle, cfg, host, rows1, 1)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"all {L} query rows x {cfg['Hq']} heads of the prefill, {reps} times "
-                      f"(fp64, OpenMP over rows)",
+            "sample": f"{len(rows)} evenly spaced query rows of {L} x {cfg['Hq']} heads x "
+                      f"{cfg['B']} sequences of the prefill (fp64, OpenMP over rows)",
             "single_thread": {"value": round(fl1 / dt1 / 1e12, 6), "unit": "TFLOP/s",
-                              "sample": f"{n1} evenly spaced query rows x {cfg['Hq']} heads",
+                              "sample": f"{len(rows1)} evenly spaced query rows x "
+                                        f"{cfg['Hq']} heads x {cfg['B']} sequences",
                               "seconds": round(dt1, 2)}}
 
 
@@ -663,23 +753,21 @@ def run_reference(args):
     host = make_step_inputs(cfg, 1, None)[0]
     import oracle
     cores = os.cpu_count() or 1
-    L, w, s = cfg["L"], cfg["w"], cfg["s"]
+    L = cfg["L"]
     rows_per_step = max(8, int(args.ref_rows))
     rng = np.random.default_rng(1)
-    sc = 1.0 / math.sqrt(cfg["d"])
     for _ in range(args.warmup):
         r = np.sort(rng.choice(L, size=min(L, 8), replace=False)).astype(np.int64)
-        oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=r, nthreads=cores)
+        _oracle_rows_timed(oracle, cfg, host, r, cores)
     total_t, total_flops = 0.0, 0.0
     for _ in range(args.steps):
         r = np.sort(rng.choice(L, size=min(L, rows_per_step), replace=False)).astype(np.int64)
-        t0 = time.perf_counter()
-        oracle.prefill(host["q"], host["k"], host["v"], w, s, sc, rows=r, nthreads=cores)
-        total_t += time.perf_counter() - t0
-        total_flops += 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * sum(keys_of_row(int(t), w, s)
-                                                                     for t in r)
+        dt, fl = _oracle_rows_timed(oracle, cfg, host, r, cores)
+        total_t += dt
+        total_flops += fl
     value = total_flops / total_t / 1e12
-    sample = f"{rows_per_step} random query rows x {cfg['Hq']} heads per step (fp64 oracle)"
+    sample = (f"{rows_per_step} random query rows x {cfg['Hq']} heads x {cfg['B']} sequences "
+              f"per step (fp64 oracle)")
     return {
         "impl": "reference",
         "metric": "SWA(w,s) prefill in-band TFLOP/s & decode KV GB/s, % of B300 roofline",
@@ -688,7 +776,10 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q/k/v, sink keys x4)",
         "config": {"workload": cfg["name"], "B": cfg["B"], "L": cfg["L"], "Hq": cfg["Hq"],
-                   "Hkv": cfg["Hkv"], "d": cfg["d"], "w": cfg["w"], "s": cfg["s"]},
+                   "Hkv": cfg["Hkv"], "d": cfg["d"], "w": cfg["w"], "s": cfg["s"],
+                   "global_batch": cfg["B"] * world, "seq_len": cfg["L"],
+                   "parallelism": f"replicas x{world}",
+                   "step": "prefill rows of the step (sampled)"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -699,17 +790,18 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--traffic", type=float, default=PREFILL_TRAFFIC_BYTES,
-                    help="DRAM bytes per prefill launch from an ncu capture of this kernel")
+    ap.add_argument("--loop-seconds", type=float, default=1.0,
+                    help="device time of each kernel's own timing loop")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--clocks-csv", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed region here")
-    ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
+    ap.add_argument("--skip-llama", action="store_true", help="omit the Llama-shaped layer loop")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
     ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions",
                                            "chunked", "paged-decode"),

@@ -250,6 +250,22 @@ SWA_API int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int r
 SWA_API int swa_keymask_host(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,
                      uint32_t *bits, int *counts);
 
+/* Test aid: swa_decode (same arguments, workspace and result) with each wait
+ * for the staged cache rows limited to wait_ns nanoseconds. With stall != 0 no
+ * copy is issued at all, so every such wait runs out: the kernel then records
+ * the wait timeout (code 1) in the device error word, writes nothing to out or
+ * the workspace, and returns; the context stays usable. Used to exercise the
+ * failure path without faulting the device. */
+SWA_API int swa_debug_decode_timeout(const void *q, const void *kcache, const void *vcache,
+                                     const int *pos, void *out, int B, int Hq, int Hkv, int d,
+                                     int w, int s, float scale, void *workspace,
+                                     size_t workspace_bytes, unsigned long long wait_ns, int stall,
+                                     swa_stream_t stream);
+
+/* (Outside this test aid, a decode whose wait runs out also records code 1 and
+ * writes nothing from the CTAs concerned; when the cache is split over CTAs the
+ * combine step still runs, so out is then undefined. Check the error word.) */
+
 /* Read the device error word that kernels set instead of trapping (a bounded
  * wait that gave up, a negative position). *code receives 0 if no error was
  * recorded. Synchronises the current device. clear != 0 resets it to 0. */

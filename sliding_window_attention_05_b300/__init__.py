@@ -74,6 +74,9 @@ _lib.swa_paged_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, 
                                   _f, _vp, _sz, _vp]
 _lib.swa_decode_noalloc.restype = _i
 _lib.swa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.swa_debug_decode_timeout.restype = _i
+_lib.swa_debug_decode_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp,
+                                          _sz, ctypes.c_ulonglong, _i, _vp]
 _lib.swa_cache_slot.restype = ctypes.c_longlong
 _lib.swa_cache_slot.argtypes = [ctypes.c_longlong, _i, _i]
 _lib.swa_cache_bytes.restype = _sz

@@ -223,14 +223,28 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
 
 // ------------------------------------------------------------------ decode
 
+// SM count of the current device (the decode split policy depends on it), or
+// 148 (a full B300) when no device is usable, so that a workspace-size query
+// without a device still answers.
+int decode_sms() {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 148;
+  }
+  DeviceInfo dev;
+  if (current_device_info(&dev) != SWA_OK || dev.sms < 1) return 148;
+  return dev.sms;
+}
+
 // Query heads one decode CTA packs: the largest of 4, 2, 1 that divides G.
 // When the (sequence, KV head) pairs are too few to fill the GPU and the
 // cache is short (cap = s + w slots, too few to split), one head per CTA
 // instead: the K/V rows a group shares are then read again, from L2. A long
 // cache is split over CTAs instead, and every K/V row is read once.
-int head_group(int B, int Hq, int Hkv, long long cap) {
+int head_group(int B, int Hq, int Hkv, long long cap, int sms) {
   const int G = Hq / Hkv;
-  if ((long long)B * Hkv * 2 < 148 && cap <= 512) return 1;
+  if ((long long)B * Hkv * 2 < sms && cap <= 512) return 1;
   if (G % 4 == 0) return 4;
   if (G % 2 == 0) return 2;
   return 1;
@@ -243,15 +257,15 @@ int head_group(int B, int Hq, int Hkv, long long cap) {
 // and one CTA's copies overlap another's arithmetic, and there are at least
 // two CTAs per SM where the cache allows 64 slots each. The count is fixed
 // from the capacity s + w (positions are only known on the device).
-int decode_splits(int B, int Hq, int Hkv, int w, int s) {
+int decode_splits(int B, int Hq, int Hkv, int w, int s, int sms) {
   const int G = Hq / Hkv;
   const long long cap = (long long)s + w;
-  const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv, cap));
+  const long long units = (long long)B * Hkv * (G / head_group(B, Hq, Hkv, cap, sms));
   long long sp = (cap + swa::kDecodeMaxKeys - 1) / swa::kDecodeMaxKeys;
-  if (units < 148 && cap > 512) {
+  if (units < sms && cap > 512) {
     const long long fine = (cap + 127) / 128;
     if (fine > sp) sp = fine;
-    long long fill = (296 + units - 1) / units;
+    long long fill = (2LL * sms + units - 1) / units;
     const long long most = (cap + 63) / 64;
     if (fill > most) fill = most;
     if (fill > sp) sp = fill;
@@ -263,8 +277,8 @@ int decode_max_keys(int w, int s, int splits) {
   return (int)(((long long)s + w + splits - 1) / splits);
 }
 
-size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
-  const int sp = decode_splits(B, Hq, Hkv, w, s);
+size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s, int sms) {
+  const int sp = decode_splits(B, Hq, Hkv, w, s, sms);
   if (sp <= 1) return 0;
   const size_t n = (size_t)B * Hq * sp;
   return n * d * sizeof(float) + n * sizeof(float2);
@@ -272,6 +286,7 @@ size_t decode_workspace(int B, int Hq, int Hkv, int d, int w, int s) {
 
 template <int D, int HG, bool kPaged>
 cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
+  // (B * Hq * splits <= INT_MAX is checked by the caller)
   const int G = a.Hq / a.Hkv;
   const size_t smem = swa::DecodeSmem<D, HG>::bytes(a.max_keys);
   const cudaError_t attr_err = ensure_max_dynamic_smem(
@@ -281,14 +296,16 @@ cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream
   dim3 grid(a.splits, a.Hkv * (G / HG), B);
   cudaError_t e = launch_pdl(swa::swa_decode_kernel<D, HG, kPaged>, grid,
                              dim3(swa::kDecodeThreads), smem, stream, a);
-  if (e != cudaSuccess || a.splits == 1) return e;
-  return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(B * a.Hq), dim3(D), 0, stream,
+  // (a stalled test launch writes no partials, so there is nothing to combine)
+  if (e != cudaSuccess || a.splits == 1 || a.stall) return e;
+  const unsigned combine_ctas = (unsigned)((long long)B * a.Hq);
+  return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(combine_ctas), dim3(D), 0, stream,
                     a.part_o, a.part_ml, a.out, a.splits);
 }
 
 template <int D, bool kPaged>
-cudaError_t launch_decode_p(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
-  switch (head_group(B, a.Hq, a.Hkv, (long long)a.w + a.s)) {
+cudaError_t launch_decode_p(const swa::DecodeArgs &a, int B, int sms, cudaStream_t stream) {
+  switch (head_group(B, a.Hq, a.Hkv, (long long)a.w + a.s, sms)) {
     case 4: return launch_decode_t<D, 4, kPaged>(a, B, stream);
     case 2: return launch_decode_t<D, 2, kPaged>(a, B, stream);
     default: return launch_decode_t<D, 1, kPaged>(a, B, stream);
@@ -296,9 +313,9 @@ cudaError_t launch_decode_p(const swa::DecodeArgs &a, int B, cudaStream_t stream
 }
 
 template <int D>
-cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, cudaStream_t stream) {
-  return a.page_table ? launch_decode_p<D, true>(a, B, stream)
-                      : launch_decode_p<D, false>(a, B, stream);
+cudaError_t launch_decode_d(const swa::DecodeArgs &a, int B, int sms, cudaStream_t stream) {
+  return a.page_table ? launch_decode_p<D, true>(a, B, sms, stream)
+                      : launch_decode_p<D, false>(a, B, sms, stream);
 }
 
 int check_heads(int Hq, int Hkv) {
@@ -319,23 +336,59 @@ int check_scale(float scale) {
 // it until exit; calls that overlap on the GPU share (and race on) it.
 static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[SWA_DECODE_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (cudaGetSymbolAddress needs that device current).
+// The current CUDA context's unique id (0 if there is none yet), through the
+// driver entry points looked up at run time. The id changes whenever a
+// context is created again (for example after cudaDeviceReset), so it tells a
+// stale scratch address from a valid one.
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current context. It is looked up
+// once per context (cudaGetSymbolAddress needs the device current, and the
+// array moves when the module is loaded again in a new context, e.g. after a
+// device reset).
 int noalloc_scratch_ptr(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(SWA_ERR_DEVICE, "device ordinal %d out of range", dev);
   static std::mutex mu;
-  static void *ptrs[64] = {nullptr};
+  static std::map<unsigned long long, void *> ptrs;  // context id -> address
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-    ptrs[dev] = p;
+  unsigned long long id = current_context_id();
+  if (id != 0) {
+    const auto it = ptrs.find(id);
+    if (it != ptrs.end()) {
+      *out = it->second;
+      return SWA_OK;
+    }
   }
-  *out = ptrs[dev];
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);  // makes the primary context current
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+  if (id == 0) id = current_context_id();
+  if (id != 0) ptrs[id] = p;
+  *out = p;
   return SWA_OK;
 }
 
@@ -544,14 +597,15 @@ int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void 
 
 size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || !supported_d(d)) return 0;
-  return decode_workspace(B, Hq, Hkv, d, w, s);
+  return decode_workspace(B, Hq, Hkv, d, w, s, decode_sms());
 }
 
 int decode_impl(const void *q, const void *k_new, const void *v_new, const void *kcache,
                 const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
                 int w, int s, float scale, void *workspace, size_t workspace_bytes,
                 swa_stream_t stream, const int *page_table = nullptr, int page_size = 0,
-                int max_pages = 0, int n_pages = 0);
+                int max_pages = 0, int n_pages = 0,
+                unsigned long long wait_ns = swa::kDecodeWaitNs, int stall = 0);
 
 int swa_decode(const void *q, const void *kcache, const void *vcache, const int *pos, void *out,
                int B, int Hq, int Hkv, int d, int w, int s, float scale, void *workspace,
@@ -575,7 +629,7 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
                 const void *vcache, const int *pos, void *out, int B, int Hq, int Hkv, int d,
                 int w, int s, float scale, void *workspace, size_t workspace_bytes,
                 swa_stream_t stream, const int *page_table, int page_size, int max_pages,
-                int n_pages) {
+                int n_pages, unsigned long long wait_ns, int stall) {
   if (!q || !kcache || !vcache || !pos || !out) return fail(SWA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
     return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -586,7 +640,13 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
   if ((rc = check_scale(scale))) return rc;
   if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
   if (B > 65535 || Hq > 65535) return fail(SWA_ERR_UNSUPPORTED, "B or Hq > 65535");
-  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s);
+  // the split policy (and so the workspace) depends on the current device's SM count
+  const int sms = decode_sms();
+  const int splits = decode_splits(B, Hq, Hkv, w, s, sms);
+  if ((long long)B * Hq * splits > 0x7FFFFFFFLL)
+    return fail(SWA_ERR_UNSUPPORTED, "B * Hq * splits (%d * %d * %d) is beyond the grid limit", B,
+                Hq, splits);
+  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s, sms);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return fail(SWA_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required, got %zu",
                 need, workspace ? workspace_bytes : (size_t)0);
@@ -606,20 +666,23 @@ int decode_impl(const void *q, const void *k_new, const void *v_new, const void 
   a.Hkv = Hkv;
   a.w = w;
   a.s = s;
-  a.splits = decode_splits(B, Hq, Hkv, w, s);
+  a.splits = splits;
   a.max_keys = decode_max_keys(w, s, a.splits);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.page_table = page_table;
   a.page_size = page_size;
   a.max_pages = max_pages;
   a.n_pages = n_pages;
+  a.wait_ns = wait_ns;
+  a.stall = stall;
   const size_t n = (size_t)B * Hq * a.splits;
   a.part_o = a.splits > 1 ? reinterpret_cast<float *>(workspace) : nullptr;
   a.part_ml = a.splits > 1 ? reinterpret_cast<float2 *>(reinterpret_cast<char *>(workspace) +
                                                         n * d * sizeof(float))
                            : nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = d == 64 ? launch_decode_d<64>(a, B, st) : launch_decode_d<128>(a, B, st);
+  cudaError_t e = d == 64 ? launch_decode_d<64>(a, B, sms, st)
+                          : launch_decode_d<128>(a, B, sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "swa_decode launch");
   return SWA_OK;
 }
@@ -630,7 +693,7 @@ int swa_decode_noalloc(const void *q, const void *kcache, const void *vcache, co
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || !supported_d(d))
     return swa_decode(q, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale, nullptr, 0,
                       stream);  // let swa_decode report the argument error
-  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s);
+  const size_t need = decode_workspace(B, Hq, Hkv, d, w, s, decode_sms());
   if (need > SWA_DECODE_NOALLOC_SCRATCH_BYTES)
     return fail(SWA_ERR_UNSUPPORTED,
                 "swa_decode_noalloc: these sizes need %zu bytes of scratch, above its fixed "
@@ -792,6 +855,14 @@ int swa_paged_decode(const void *q, const void *kpool, const void *vpool, const 
   return decode_impl(q, nullptr, nullptr, kpool, vpool, pos, out, B, Hq, Hkv, d, w, s, scale,
                      workspace, workspace_bytes, stream, page_table, page_size, max_pages,
                      n_pages);
+}
+
+int swa_debug_decode_timeout(const void *q, const void *kcache, const void *vcache,
+                             const int *pos, void *out, int B, int Hq, int Hkv, int d, int w,
+                             int s, float scale, void *workspace, size_t workspace_bytes,
+                             unsigned long long wait_ns, int stall, swa_stream_t stream) {
+  return decode_impl(q, nullptr, nullptr, kcache, vcache, pos, out, B, Hq, Hkv, d, w, s, scale,
+                     workspace, workspace_bytes, stream, nullptr, 0, 0, 0, wait_ns, stall);
 }
 
 int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int nrows,

@@ -83,3 +83,10 @@ def test_cache_append_rejects_shapes():
     with pytest.raises(ValueError, match="v_new"):
         swa.swa_cache_append(kn, _t(B, 4, Hkv, d), kc, kc.clone(),
                              torch.zeros(B, dtype=torch.int32), w, s)
+
+
+def test_fa_decode_layer_needs_max_len():
+    with pytest.raises(ValueError, match="max_len"):
+        swa.AttentionLayer(1, 4, 1, 64, 16, 4, fa_decode=True)
+    with pytest.raises(ValueError, match="max_len"):
+        swa.HybridStack(1, 4, 1, 64, [(16, 4), (40, 0)], fa_decode=True)
