@@ -108,7 +108,6 @@ __global__ void swa_paged_append_kernel(const uint4 *__restrict__ k_new,
 // ---------------------------------------------------------------- decode
 
 constexpr int kDecodeThreads = 128;
-constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kDecodeMaxKeys = 256;   // slots one CTA stages (128 KB of K+V at d = 128)
 constexpr int kDecodeMaxHeads = 4;    // query heads one CTA packs
 constexpr uint64_t kDecodeWaitNs = 2000000000ull;   // bounded wait for the staged data
@@ -150,28 +149,18 @@ struct DecodeArgs {
   int stall;
 };
 
-// Dynamic shared memory of one decode CTA:
-//   barriers   K and V barrier of each warp
-//   sK, sV     [max_keys][D] bf16 staged rows
-//   sS         [max_keys][HG] fp32 scores (unscaled)
-//   sP         [max_keys][HG] float2 (p, p): the weight twice, so that the
-//              value product takes a ready operand pair
-//   sO         [warps][HG][D] fp32 partial outputs
-//   sQ         [HG][D] fp32 query rows
-//   sML        [warps][HG] float2 (max, sum)
-// (every region starts on a 16-byte boundary)
+constexpr int kDecodeChunk = kDecodeMaxKeys;  // keys per chunk: one chunk per CTA
+constexpr int kDecodeMaxChunks = kDecodeMaxKeys / kDecodeChunk;
+
+// Dynamic shared memory of one decode CTA.
 template <int D, int HG>
 struct DecodeSmem {
-  static constexpr size_t kBar = 128;
-  __host__ __device__ static constexpr size_t up16(size_t x) { return (x + 15) & ~size_t(15); }
-  __host__ __device__ static size_t k_off() { return kBar; }
-  __host__ __device__ static size_t v_off(int mk) { return k_off() + up16((size_t)mk * D * 2); }
-  __host__ __device__ static size_t s_off(int mk) { return v_off(mk) + up16((size_t)mk * D * 2); }
-  __host__ __device__ static size_t p_off(int mk) { return s_off(mk) + up16((size_t)mk * HG * 4); }
-  __host__ __device__ static size_t o_off(int mk) { return p_off(mk) + up16((size_t)mk * HG * 8); }
-  __host__ __device__ static size_t q_off(int mk) { return o_off(mk) + up16((size_t)kDecodeWarps * HG * D * 4); }
-  __host__ __device__ static size_t ml_off(int mk) { return q_off(mk) + up16((size_t)HG * D * 4); }
-  __host__ __device__ static size_t bytes(int mk) { return 128 /* alignment */ + ml_off(mk) + kDecodeWarps * HG * 8; }
+  static size_t bytes(int max_keys) {
+    return 128 /* alignment */ + 256 /* barriers */ + 2 * (size_t)max_keys * D * 2 +
+           2 * (size_t)(max_keys < kDecodeChunk ? max_keys : kDecodeChunk) * HG * 4 /* P */ +
+           3 * HG * 4 + 16 +
+           (size_t)kDecodeThreads * HG * 8;
+  }
 };
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -188,94 +177,45 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Issue the bulk copies of one warp's keys [j_lo, j_hi) (keys numbered from
-// the CTA's first key k_begin; paged: the positions of K(pos) in order, the
-// sinks then pos - w + 1 .. pos, one copy per run inside a page). Returns
-// false, with nothing issued, when a page is unmapped or out of range.
-template <int D, bool kPaged>
-__device__ __forceinline__ bool decode_issue(const DecodeArgs &a, int b, int kvh, int pos,
-                                             int k_begin, int j_lo, int j_hi,
-                                             __nv_bfloat16 *sK, __nv_bfloat16 *sV,
-                                             uint64_t *bar_k, uint64_t *bar_v) {
-  const uint32_t bytes = (uint32_t)(j_hi - j_lo) * D * 2;
-  if constexpr (kPaged) {
-    const int ns = imin(a.s, pos + 1);              // sink positions held
-    const long long lo = imax(a.s, pos - a.w + 1);  // first window position
-    const int *tbl = a.page_table + (size_t)b * a.max_pages;
-    for (int pass = 0; pass < 2; ++pass) {          // check every page, then copy
-      if (pass == 1) {
-        mbar_arrive_expect_tx(bar_k, bytes);
-        mbar_arrive_expect_tx(bar_v, bytes);
-      }
-      for (int i = k_begin + j_lo; i < k_begin + j_hi;) {
-        const long long p = i < ns ? i : lo + (i - ns);
-        const int seg_end = i < ns ? imin(k_begin + j_hi, ns) : k_begin + j_hi;
-        const long long lp = p / a.page_size;
-        const int row = (int)(p % a.page_size);
-        const int len = imin(seg_end - i, a.page_size - row);
-        const int page = lp < a.max_pages ? tbl[lp] : -1;
-        if (page < 0 || page >= a.n_pages) return false;
-        if (pass == 1) {
-          const size_t src = (((size_t)page * a.Hkv + kvh) * a.page_size + row) * D;
-          const size_t dst = (size_t)(i - k_begin) * D;
-          bulk_load(sK + dst, a.kc + src, (uint32_t)len * D * 2, bar_k);
-          bulk_load(sV + dst, a.vc + src, (uint32_t)len * D * 2, bar_v);
-        }
-        i += len;
-      }
-    }
-  } else {
-    const size_t row0 = ((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w) + k_begin + j_lo;
-    mbar_arrive_expect_tx(bar_k, bytes);
-    bulk_load(sK + (size_t)j_lo * D, a.kc + row0 * D, bytes, bar_k);
-    mbar_arrive_expect_tx(bar_v, bytes);
-    bulk_load(sV + (size_t)j_lo * D, a.vc + row0 * D, bytes, bar_v);
-  }
-  return true;
-}
-
 // HG query heads per CTA (a divisor of G, at most 4); D = head dimension.
 //
-// One CTA (4 warps) serves one (sequence, KV head, head group, split). Its
-// keys are cut into four contiguous runs, one per warp (in whole groups of 4
-// keys). Each warp stages its own run of K and of V with one bulk copy each
-// (its own barriers), so it starts as soon as its rows land, and computes, with
-// no block-wide barrier, its scores (8 lanes per key, 16 elements of d each,
-// all HG heads at once: every K element is read and converted once for the
-// group), the softmax of its keys and its share of P V (each lane 4 columns of
-// d for all HG heads). The four partial results (max, sum, O) are merged at the
-// end, or, when the cache is split over CTAs, written as one partial per split
-// for the combine kernel.
+// The CTA's slots are consumed in chunks of kDecodeChunk keys (the K and V of
+// every chunk requested at once, one bulk copy each with its own barrier) with
+// an online softmax across chunks; with kDecodeChunk = kDecodeMaxKeys a CTA
+// has a single chunk, K first and V second, so the scores start while V is
+// still arriving.
 //
-// Failure path: a wait that runs out records kErrWaitTimeout and sets the
-// CTA's abort word; a paged CTA that meets an unmapped page records
-// kErrMissingPage. Then every warp skips its arithmetic, the CTA waits
-// (bounded, not abortable) for the copies it issued, and exits without
-// writing any output.
+// kPaged: the cache is paged. The CTA's keys are then the positions of K(pos)
+// in order (the sinks, then pos - w + 1 .. pos), and each run of them inside
+// one page is one bulk copy; key order does not change the result.
 //
-// kPaged: the cache is paged (see decode_issue); key order does not change
-// the result.
+// Failure path: a wait that runs out (bounded by a.wait_ns) records
+// kErrWaitTimeout; the CTA then skips the rest of the arithmetic, waits
+// (bounded, not abortable) for the copies it issued, and exits without writing
+// anything. A stalled test launch (a.stall) issues no copy, so its waits run
+// out.
 template <int D, int HG, bool kPaged>
-__global__ void __launch_bounds__(kDecodeThreads, 4) swa_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const DecodeArgs a) {
   constexpr int LPK = 8;            // lanes per key row in the score phase
   constexpr int EPL = D / LPK;      // elements of a row per lane (16 or 8)
-  constexpr int CPL = D / 32;       // output columns per lane in the value phase (4 or 2)
-  using Smem = DecodeSmem<D, HG>;
+  constexpr int kPairs = D / 2;     // column pairs of a row
+  constexpr int kParts = kDecodeThreads / kPairs;  // key parts in the P V phase
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) &
                                              ~uintptr_t(127));
-  const int mk = a.max_keys;
-  uint64_t *bar_k = reinterpret_cast<uint64_t *>(dsm);           // [warps]
-  uint64_t *bar_v = bar_k + kDecodeWarps;                        // [warps]
-  volatile int *abort_word = reinterpret_cast<volatile int *>(bar_v + kDecodeWarps);
-  volatile int *page_fault = abort_word + 1;
-  __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(dsm + Smem::k_off());
-  __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(dsm + Smem::v_off(mk));
-  float *sS = reinterpret_cast<float *>(dsm + Smem::s_off(mk));
-  float2 *sP = reinterpret_cast<float2 *>(dsm + Smem::p_off(mk));
-  float *sO = reinterpret_cast<float *>(dsm + Smem::o_off(mk));
-  float *sQ = reinterpret_cast<float *>(dsm + Smem::q_off(mk));
-  float2 *sML = reinterpret_cast<float2 *>(dsm + Smem::ml_off(mk));
+  uint64_t *bar_k = reinterpret_cast<uint64_t *>(dsm);                  // [kDecodeMaxChunks]
+  uint64_t *bar_v = bar_k + kDecodeMaxChunks;                           // [kDecodeMaxChunks]
+  __nv_bfloat16 *sK = reinterpret_cast<__nv_bfloat16 *>(dsm + 256);     // [max_keys][D]
+  __nv_bfloat16 *sV = sK + (size_t)a.max_keys * D;                       // [max_keys][D]
+  const int pchunk = imin(kDecodeChunk, a.max_keys);                  // keys of a P buffer
+  float *sP = reinterpret_cast<float *>(sV + (size_t)a.max_keys * D);  // [2][pchunk][HG]
+  float *sM = sP + 2 * pchunk * HG;                                    // [HG] running max
+  float *sL = sM + HG;                                                 // [HG] running sum
+  float *sF = sL + HG;                                                 // [HG] rescale factor
+  float2 *sO = reinterpret_cast<float2 *>(                             // [kParts][HG][kPairs]
+      (reinterpret_cast<uintptr_t>(sF + HG) + 15) & ~uintptr_t(15));
+  __shared__ int abort_word;
+  __shared__ int missing_page;
 
   const int split = blockIdx.x;
   const int G = a.Hq / a.Hkv;
@@ -297,36 +237,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) swa_decode_kernel(const Dec
   const int per_split = cdiv(n, a.splits);
   const int k_begin = imin(n, split * per_split);
   const int nk = imin(n, k_begin + per_split) - k_begin;  // <= max_keys
-  // this warp's run of keys: whole groups of 4, spread evenly over the warps
-  const int ngroups = cdiv(nk, 4);
-  const int j_lo = imin(nk, (warp * ngroups / kDecodeWarps) * 4);
-  const int j_hi = imin(nk, ((warp + 1) * ngroups / kDecodeWarps) * 4);
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecodeWarps; ++i) {
-      mbar_init(&bar_k[i], 1);
-      mbar_init(&bar_v[i], 1);
-    }
-    *abort_word = 0;
-    *page_fault = 0;
-    fence_mbar_init();
-  }
-  // the query rows of the HG heads (contiguous in q): kQWpt bf16 pairs per
-  // thread are loaded now and converted once the copies are under way
-  constexpr int kQWords = HG * D / 2;                                     // 32 .. 256
-  constexpr int kQWpt = kQWords > kDecodeThreads ? kQWords / kDecodeThreads : 1;  // 1 or 2
-  constexpr int kQThreads = kQWords / kQWpt;
-  uint32_t qraw[2] = {0u, 0u};
-  if (threadIdx.x < kQThreads) {
-    const __nv_bfloat16 *qsrc = a.q + ((size_t)b * a.Hq + hq0) * D + threadIdx.x * kQWpt * 2;
-    if constexpr (kQWpt == 2) {
-      const uint2 u = *reinterpret_cast<const uint2 *>(qsrc);
-      qraw[0] = u.x;
-      qraw[1] = u.y;
-    } else {
-      qraw[0] = *reinterpret_cast<const uint32_t *>(qsrc);
-    }
-  }
+  const int n_chunks = cdiv(nk, kDecodeChunk);
   // With k_new: the token at position pos goes to ring slot(pos). Every CTA
   // that stages that slot patches its shared-memory copy; the first head
   // group's CTA also writes it to the cache.
@@ -346,71 +257,126 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) swa_decode_kernel(const Dec
       }
     }
   }
-  __syncthreads();  // barriers initialised
 
-  // ---- stage: lane 0 of each warp copies the warp's run of K and of V
-  int issued = 0;
-  if (lane == 0 && j_hi > j_lo && !a.stall) {
-    if (decode_issue<D, kPaged>(a, b, kvh, pos, k_begin, j_lo, j_hi, sK, sV, &bar_k[warp],
-                                &bar_v[warp])) {
-      issued = 1;
-    } else {
-      *page_fault = 1;
-      record_error(kErrMissingPage);
+  const size_t row_base = ((size_t)b * a.Hkv + kvh) * (size_t)(a.s + a.w) + k_begin;
+  if (threadIdx.x == 0) {
+    abort_word = 0;
+    missing_page = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      mbar_init(&bar_k[c], 1);
+      mbar_init(&bar_v[c], 1);
     }
+    fence_mbar_init();
   }
-  issued = __shfl_sync(0xffffffffu, issued, 0);
-  // query rows -> fp32 in shared memory
-  if (threadIdx.x < kQThreads) {
-    float *qd = sQ + threadIdx.x * kQWpt * 2;
-    if constexpr (kQWpt == 2) {
-      const float2 f0 = bf16x2_to_f2(qraw[0]), f1 = bf16x2_to_f2(qraw[1]);
-      *reinterpret_cast<float4 *>(qd) = make_float4(f0.x, f0.y, f1.x, f1.y);
-    } else {
-      *reinterpret_cast<float2 *>(qd) = bf16x2_to_f2(qraw[0]);
-    }
-  }
-  __syncthreads();
-
-  const bool mine = j_hi > j_lo && (issued || a.stall);  // this warp has rows coming
-  float m_w = -INFINITY, l_w = 0.f;                      // head lane % HG, over my keys
-  bool wrote_o = false;
-  bool ok = mine;
-  if (ok) {
-    // every lane polls; the outcome is made warp-uniform
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar_k[warp], 0, abort_word, a.wait_ns));
-  }
-  if (ok) {
-    const int kg = lane / LPK;   // which of the 4 keys of a warp step
-    const int dl = lane % LPK;   // which slice of d
-    if (append_row >= j_lo && append_row < j_hi && lane < D / 8) {
-      // the appended token's slot: its staged row still holds the old entry
-      reinterpret_cast<uint4 *>(sK + (size_t)append_row * D)[lane] =
-          reinterpret_cast<const uint4 *>(a.k_new + ((size_t)b * a.Hkv + kvh) * D)[lane];
-    }
-    // this lane's slice of the HG query rows
-    float2 q2[HG][EPL / 2];
-#pragma unroll
-    for (int h = 0; h < HG; ++h)
-#pragma unroll
-      for (int v = 0; v < EPL / 4; ++v) {
-        const float4 f = *reinterpret_cast<const float4 *>(sQ + h * D + dl * EPL + v * 4);
-        q2[h][2 * v] = make_float2(f.x, f.y);
-        q2[h][2 * v + 1] = make_float2(f.z, f.w);
+  if constexpr (kPaged) {
+    // keys k_begin .. k_begin + nk - 1 of the list [sinks | window] (one chunk:
+    // nk <= kDecodeMaxKeys); every page is checked before any copy is issued
+    if (threadIdx.x == 0 && nk > 0 && !a.stall) {
+      const int ns = imin(a.s, pos + 1);              // sink positions held
+      const long long lo = imax(a.s, pos - a.w + 1);  // first window position
+      const int *tbl = a.page_table + (size_t)b * a.max_pages;
+      for (int pass = 0; pass < 2 && !missing_page; ++pass) {
+        if (pass == 1) {
+          mbar_arrive_expect_tx(&bar_k[0], (uint32_t)nk * D * 2);
+          mbar_arrive_expect_tx(&bar_v[0], (uint32_t)nk * D * 2);
+        }
+        for (int i = k_begin; i < k_begin + nk;) {
+          const long long p = i < ns ? i : lo + (i - ns);
+          const int seg_end = i < ns ? imin(k_begin + nk, ns) : k_begin + nk;
+          const long long lp = p / a.page_size;
+          const int row = (int)(p % a.page_size);
+          const int len = imin(seg_end - i, a.page_size - row);
+          const int page = lp < a.max_pages ? tbl[lp] : -1;
+          if (page < 0 || page >= a.n_pages) {
+            missing_page = 1;
+            record_error(kErrMissingPage);
+            break;
+          }
+          if (pass == 1) {
+            const size_t src = (((size_t)page * a.Hkv + kvh) * a.page_size + row) * D;
+            const uint32_t bytes = (uint32_t)len * D * 2;
+            bulk_load(sK + (size_t)(i - k_begin) * D, a.kc + src, bytes, &bar_k[0]);
+            bulk_load(sV + (size_t)(i - k_begin) * D, a.vc + src, bytes, &bar_v[0]);
+          }
+          i += len;
+        }
       }
-    __syncwarp();
-    // ---- scores: a warp step covers 4 keys, 8 lanes per key
-    constexpr int kSpan = LPK / HG;  // lanes that end up holding one head's total
-    for (int j0 = j_lo; j0 < j_hi; j0 += 4) {
+    }
+  } else if (threadIdx.x == 0 && !a.stall) {
+    // every chunk's K first, then every chunk's V: the scores need K first
+    for (int c = 0; c < n_chunks; ++c) {
+      const int kc = imin(kDecodeChunk, nk - c * kDecodeChunk);
+      const uint32_t bytes = (uint32_t)kc * D * 2;
+      mbar_arrive_expect_tx(&bar_k[c], bytes);
+      bulk_load(sK + (size_t)c * kDecodeChunk * D, a.kc + (row_base + c * kDecodeChunk) * D,
+                bytes, &bar_k[c]);
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+      const int kc = imin(kDecodeChunk, nk - c * kDecodeChunk);
+      const uint32_t bytes = (uint32_t)kc * D * 2;
+      mbar_arrive_expect_tx(&bar_v[c], bytes);
+      bulk_load(sV + (size_t)c * kDecodeChunk * D, a.vc + (row_base + c * kDecodeChunk) * D,
+                bytes, &bar_v[c]);
+    }
+  }
+  if (threadIdx.x < HG) {
+    sM[threadIdx.x] = -INFINITY;
+    sL[threadIdx.x] = 0.f;
+  }
+  // queries of the HG heads, this lane's slice as pairs, pre-scaled to log2 units
+  const int kg = lane / LPK;   // which of the 4 keys of a warp step
+  const int dl = lane % LPK;   // which slice of d
+  float2 q2[HG][EPL / 2];
+#pragma unroll
+  for (int h = 0; h < HG; ++h) {
+#pragma unroll
+    for (int v = 0; v < EPL / 8; ++v) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.Hq + hq0 + h) * D +
+                                                         dl * EPL + v * 8);
+      const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = bf16x2_to_f2(wd[e]);
+        q2[h][v * 4 + e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+      }
+    }
+  }
+  const int cp = threadIdx.x % kPairs, part = threadIdx.x / kPairs;  // P V phase mapping
+  float2 o2[HG];
+#pragma unroll
+  for (int h = 0; h < HG; ++h) o2[h] = make_float2(0.f, 0.f);
+  __syncthreads();  // barriers initialised
+  if (kPaged && missing_page) return;  // nothing was copied
+  // chunks whose copies thread 0 has seen land, and whether a wait ran out
+  int landed = 0;
+  bool failed = false;
+
+  for (int c = 0; c < n_chunks; ++c) {
+    const int j_base = c * kDecodeChunk;
+    const int kc = imin(kDecodeChunk, nk - j_base);
+    float *sPc = sP + (c & 1) * pchunk * HG;  // [pchunk][HG]
+    // one thread polls the barrier; the others sleep in __syncthreads (which
+    // also tells every thread whether the wait ran out)
+    failed = __syncthreads_or(threadIdx.x == 0 && !mbar_wait(&bar_k[c], 0, &abort_word, a.wait_ns));
+    if (failed) break;
+    if (append_row >= j_base && append_row < j_base + kc) {
+      // the appended token's slot: its staged row still holds the old entry
+      if (threadIdx.x < D / 8)
+        reinterpret_cast<uint4 *>(sK + (size_t)append_row * D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(a.k_new + ((size_t)b * a.Hkv + kvh) * D)[threadIdx.x];
+      __syncthreads();
+    }
+    // ---- scores of the chunk: each warp step covers 4 keys, 8 lanes per key
+    for (int j0 = warp * 4; j0 < kc; j0 += 4 * (kDecodeThreads / 32)) {
       const int j = j0 + kg;
       float2 acc2[HG];
 #pragma unroll
       for (int h = 0; h < HG; ++h) acc2[h] = make_float2(0.f, 0.f);
-      if (j < j_hi) {
+      if (j < kc) {
 #pragma unroll
         for (int v = 0; v < EPL / 8; ++v) {
           const uint4 raw =
-              *reinterpret_cast<const uint4 *>(sK + (size_t)j * D + dl * EPL + v * 8);
+              *reinterpret_cast<const uint4 *>(sK + (size_t)(j_base + j) * D + dl * EPL + v * 8);
           const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -420,162 +386,111 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) swa_decode_kernel(const Dec
           }
         }
       }
-      // reduce over the 8 lanes of the key, scattering the heads: lane dl ends
-      // with the total of head dl / kSpan
-      float tot;
-      if constexpr (HG == 4) {
-        const float a0 = acc2[0].x + acc2[0].y, a1 = acc2[1].x + acc2[1].y;
-        const float a2 = acc2[2].x + acc2[2].y, a3 = acc2[3].x + acc2[3].y;
-        const bool b2 = (dl & 4) != 0, b1 = (dl & 2) != 0;
-        float k0 = b2 ? a2 : a0, k1 = b2 ? a3 : a1;
-        const float s0 = b2 ? a0 : a2, s1 = b2 ? a1 : a3;
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
-        tot = b1 ? k1 : k0;
-        tot += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
-        tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-      } else if constexpr (HG == 2) {
-        const float a0 = acc2[0].x + acc2[0].y, a1 = acc2[1].x + acc2[1].y;
-        const bool b2 = (dl & 4) != 0;
-        tot = b2 ? a1 : a0;
-        tot += __shfl_xor_sync(0xffffffffu, b2 ? a0 : a1, 4);
-        tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-        tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-      } else {
-        tot = acc2[0].x + acc2[0].y;
-        tot += __shfl_xor_sync(0xffffffffu, tot, 4);
-        tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-        tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-      }
-      if (j < j_hi && (dl % kSpan) == 0) sS[j * HG + dl / kSpan] = tot;
-    }
-    __syncwarp();
-    // ---- softmax over my keys: lane = r * HG + h
-    {
-      constexpr int R = 32 / HG;
-      const int h = lane % HG, r = lane / HG;
-      float mx = -INFINITY;
-      for (int j = j_lo + r; j < j_hi; j += R) mx = fmaxf(mx, sS[j * HG + h]);
+      float acc[HG];
 #pragma unroll
-      for (int off = HG; off < 32; off *= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      m_w = mx * a.scale_log2;           // scale > 0: the max commutes with it
+      for (int h = 0; h < HG; ++h) acc[h] = acc2[h].x + acc2[h].y;
+#pragma unroll
+      for (int off = LPK / 2; off >= 1; off /= 2)
+#pragma unroll
+        for (int h = 0; h < HG; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
+      if (dl == 0 && j < kc) {
+#pragma unroll
+        for (int h = 0; h < HG; ++h) sPc[j * HG + h] = acc[h];
+      }
+    }
+    __syncthreads();
+    // ---- online softmax update of each head (warp h)
+    if (warp < HG) {
+      float mc = -INFINITY;
+      for (int j = lane; j < kc; j += 32) mc = fmaxf(mc, sPc[j * HG + warp]);
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+      const float m_old = sM[warp];
+      const float m_new = fmaxf(m_old, mc);
       float ls = 0.f;
-      for (int j = j_lo + r; j < j_hi; j += R) {
-        const float p = fast_exp2(fmaf(sS[j * HG + h], a.scale_log2, -m_w));
-        sP[j * HG + h] = make_float2(p, p);
+      for (int j = lane; j < kc; j += 32) {
+        const float p = fast_exp2(sPc[j * HG + warp] - m_new);
+        sPc[j * HG + warp] = p;
         ls += p;
       }
 #pragma unroll
-      for (int off = HG; off < 32; off *= 2) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-      l_w = ls;
-    }
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar_v[warp], 0, abort_word, a.wait_ns));
-    if (ok) {
-      if (append_row >= j_lo && append_row < j_hi && lane < D / 8) {
-        reinterpret_cast<uint4 *>(sV + (size_t)append_row * D)[lane] =
-            reinterpret_cast<const uint4 *>(a.v_new + ((size_t)b * a.Hkv + kvh) * D)[lane];
+      for (int off = 16; off >= 1; off /= 2) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      if (lane == 0) {
+        const float f = m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new);
+        sF[warp] = f;
+        sM[warp] = m_new;
+        sL[warp] = sL[warp] * f + ls;
       }
-      __syncwarp();
-      // ---- O += P V over my keys: lane = CPL consecutive columns, all heads
-      float2 o2[HG][CPL / 2];
+    }
+    failed = __syncthreads_or(threadIdx.x == 0 && !mbar_wait(&bar_v[c], 0, &abort_word, a.wait_ns));
+    if (failed) break;
+    landed = c + 1;
+    if (append_row >= j_base && append_row < j_base + kc) {
+      if (threadIdx.x < D / 8)
+        reinterpret_cast<uint4 *>(sV + (size_t)append_row * D)[threadIdx.x] =
+            reinterpret_cast<const uint4 *>(a.v_new + ((size_t)b * a.Hkv + kvh) * D)[threadIdx.x];
+      __syncthreads();
+    }
+    // ---- O = O * f + P V over the chunk: thread = (column pair, key part);
+    // one V pair feeds all HG heads (consecutive threads: consecutive pairs)
+    {
+      float f[HG];
 #pragma unroll
-      for (int h = 0; h < HG; ++h)
+      for (int h = 0; h < HG; ++h) f[h] = sF[h];
 #pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) o2[h][c] = make_float2(0.f, 0.f);
-      const __nv_bfloat16 *vcol = sV + lane * CPL;
-#pragma unroll 2
+      for (int h = 0; h < HG; ++h) o2[h] = make_float2(o2[h].x * f[h], o2[h].y * f[h]);
+      const int per_part = cdiv(kc, kParts);
+      const int j_lo = imin(kc, part * per_part), j_hi = imin(kc, j_lo + per_part);
+      const uint32_t *vcol = reinterpret_cast<const uint32_t *>(sV + (size_t)j_base * D) + cp;
       for (int j = j_lo; j < j_hi; ++j) {
-        float2 vf[CPL / 2];
-        if constexpr (CPL == 4) {
-          const uint2 u = *reinterpret_cast<const uint2 *>(vcol + (size_t)j * D);
-          vf[0] = bf16x2_to_f2(u.x);
-          vf[1] = bf16x2_to_f2(u.y);
+        const float2 vf = bf16x2_to_f2(vcol[(size_t)j * kPairs]);
+        float pr[HG];
+        if constexpr (HG == 4) {
+          const float4 p4 = *reinterpret_cast<const float4 *>(sPc + j * 4);
+          pr[0] = p4.x; pr[1] = p4.y; pr[2] = p4.z; pr[3] = p4.w;
         } else {
-          vf[0] = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(vcol + (size_t)j * D));
-        }
-        float2 pr[HG];
-        if constexpr (HG >= 2) {
 #pragma unroll
-          for (int h = 0; h < HG; h += 2) {
-            const float4 p4 = *reinterpret_cast<const float4 *>(sP + j * HG + h);
-            pr[h] = make_float2(p4.x, p4.y);
-            pr[h + 1] = make_float2(p4.z, p4.w);
-          }
-        } else {
-          pr[0] = sP[j];
+          for (int h = 0; h < HG; ++h) pr[h] = sPc[j * HG + h];
         }
 #pragma unroll
-        for (int h = 0; h < HG; ++h)
-#pragma unroll
-          for (int c = 0; c < CPL / 2; ++c) o2[h][c] = ffma2(pr[h], vf[c], o2[h][c]);
+        for (int h = 0; h < HG; ++h) o2[h] = ffma2(make_float2(pr[h], pr[h]), vf, o2[h]);
       }
-      // the warp's partial O -> shared memory
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        float *dst = sO + ((size_t)warp * HG + h) * D + lane * CPL;
-        if constexpr (CPL == 4)
-          *reinterpret_cast<float4 *>(dst) =
-              make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-        else
-          *reinterpret_cast<float2 *>(dst) = o2[h][0];
+    }
+    // the next chunk writes the other P buffer; the one after that reuses
+    // this one only after the next chunk's barrier
+  }
+  if (failed || a.stall) {
+    // failure path: every copy issued lands before the CTA exits (bounded, not
+    // abortable), and nothing is written
+    if (threadIdx.x == 0 && !a.stall) {
+      for (int c = landed; c < n_chunks; ++c) {
+        mbar_wait(&bar_k[c], 0, &abort_word, kDecodeDrainNs, false);
+        mbar_wait(&bar_v[c], 0, &abort_word, kDecodeDrainNs, false);
       }
-      wrote_o = true;
-    }
-  }
-  if (!ok) {
-    m_w = -INFINITY;
-    l_w = 0.f;
-  }
-  if (!wrote_o) {
-    // no keys, or a failed wait: an empty partial
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      float *dst = sO + ((size_t)warp * HG + h) * D + lane * CPL;
-      if constexpr (CPL == 4)
-        *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-      else
-        *reinterpret_cast<float2 *>(dst) = make_float2(0.f, 0.f);
-    }
-  }
-  // ---- the warp's (max, sum) -> shared memory
-  if (lane < HG) sML[warp * HG + lane] = make_float2(m_w, l_w);
-  __syncthreads();
-  if (*abort_word || *page_fault || a.stall) {
-    // failure path: let this warp's copies land before the CTA exits; write nothing
-    if (lane == 0 && issued) {
-      mbar_wait(&bar_k[warp], 0, abort_word, kDecodeDrainNs, false);
-      mbar_wait(&bar_v[warp], 0, abort_word, kDecodeDrainNs, false);
     }
     return;
   }
-  // ---- merge the warps' partials: thread = (head, column pair)
-  for (int item = threadIdx.x; item < HG * (D / 2); item += kDecodeThreads) {
-    const int h = item / (D / 2), cp = item % (D / 2);
-    float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sML[w * HG + h].x);
-    float2 o = make_float2(0.f, 0.f);
-    float den = 0.f;
-    if (M != -INFINITY) {
+  for (int h = 0; h < HG; ++h) sO[(part * HG + h) * kPairs + cp] = o2[h];
+  __syncthreads();
+  for (int item = threadIdx.x; item < HG * kPairs; item += kDecodeThreads) {
+    const int h = item / kPairs, cq = item % kPairs;
+    float2 o = sO[h * kPairs + cq];
 #pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float2 ml = sML[w * HG + h];
-        const float f = fast_exp2(ml.x - M);   // 0 for a warp without keys
-        const float2 x = reinterpret_cast<const float2 *>(sO + ((size_t)w * HG + h) * D)[cp];
-        o.x = fmaf(f, x.x, o.x);
-        o.y = fmaf(f, x.y, o.y);
-        den = fmaf(f, ml.y, den);
-      }
+    for (int pp = 1; pp < kParts; ++pp) {
+      const float2 x = sO[(pp * HG + h) * kPairs + cq];
+      o.x += x.x;
+      o.y += x.y;
     }
     const int hq = hq0 + h;
     if (a.splits == 1) {
-      const float inv = 1.0f / den;
-      reinterpret_cast<uint32_t *>(a.out + ((size_t)b * a.Hq + hq) * D)[cp] =
+      const float inv = 1.0f / sL[h];
+      reinterpret_cast<uint32_t *>(a.out + ((size_t)b * a.Hq + hq) * D)[cq] =
           pack_bf16x2(o.x * inv, o.y * inv);
     } else {
       const size_t pi = ((size_t)b * a.Hq + hq) * a.splits + split;
-      reinterpret_cast<float2 *>(a.part_o + pi * D)[cp] = o;
-      if (cp == 0) a.part_ml[pi] = make_float2(M, den);
+      reinterpret_cast<float2 *>(a.part_o + pi * D)[cq] = o;
+      if (cq == 0) a.part_ml[pi] = nk > 0 ? make_float2(sM[h], sL[h]) : make_float2(-INFINITY, 0.f);
     }
   }
 }

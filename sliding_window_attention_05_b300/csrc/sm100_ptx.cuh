@@ -91,7 +91,8 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, vola
     if (mbar_try_wait(bar, parity)) return true;
     if ((++it & 63u) == 0) {
       if (abortable && *abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) {
+      // (the iteration cap is a second bound, in case the timer does not advance)
+      if (global_timer_ns() - t0 > timeout_ns || it > (1u << 30)) {
         *abort = 1;
         record_error(kErrWaitTimeout);
         return false;
