@@ -656,6 +656,42 @@ def bench_paged_decode(swa, device, stream, peaks, iters=64, page_size=64):
              "l2": f"{ncache} caches in one pool of {pool.n_pages} pages"}]
 
 
+def bench_backward(swa, device, stream, peaks, iters=5):
+    """Backward of the prefill (dq, dk, dv from dout) on the Llama-shaped layer
+    (B=1, L=4096, SWA(128, 4)) and the long-window case (B=2, L=32768,
+    SWA(512, 4)). In-band FLOPs of the backward: 10 d per admitted (row, key)
+    pair and query head (S, dP, dV, dK and dQ products; the kernels recompute
+    S and dP once more, which is not counted)."""
+    lines = []
+    for (B, L, w, s, seed) in ((1, 4096, 128, 4, 1002), (2, 32768, 512, 4, 1004)):
+        Hq, Hkv, d = 32, 8, 128
+        q, k, v = (t.to(device) for t in swa_inputs.prefill_inputs(B, L, Hq, Hkv, d, seed,
+                                                                    sink_rows=4))
+        g = torch.Generator(device=device).manual_seed(seed + 1)
+        dout = torch.randn(B, L, Hq, d, generator=g, device=device).to(torch.bfloat16)
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=device)
+        out = torch.empty_like(q)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(swa.swa_prefill_backward_workspace_size(B, L, Hq, Hkv, d, s),
+                         dtype=torch.uint8, device=device)
+        fwd_ms = _time_events(lambda: swa.swa_prefill(q, k, v, w, s, out=out, lse=lse), stream,
+                              iters)
+        bwd_ms = _time_events(lambda: swa.swa_prefill_backward(q, k, v, out, dout, lse, w, s,
+                                                               dq=dq, dk=dk, dv=dv, workspace=ws),
+                              stream, iters)
+        pairs = pairs_per_head(L, w, s)
+        fl = 10.0 * B * Hq * d * pairs
+        lines.append({"workload": f"prefill backward SWA({w},{s}) B={B} L={L} Hq={Hq} Hkv={Hkv} "
+                                  f"d={d}",
+                      "forward_with_lse_us": round(fwd_ms * 1e3, 1),
+                      "backward_us": round(bwd_ms * 1e3, 1),
+                      "backward_tflops": round(fl / (bwd_ms * 1e-3) / 1e12, 1),
+                      "backward_tensor_frac": round(fl / (bwd_ms * 1e-3) / 1e12 /
+                                                    peaks["bf16_tflops"], 4),
+                      "inband_flop": fl, "iters": iters})
+    return lines
+
+
 def run_other(args):
     import sliding_window_attention_05_b300 as swa
     device = torch.device("cuda", 0)
@@ -664,7 +700,7 @@ def run_other(args):
     peaks = load_peaks()
     fn = {"window-sweep": bench_window_sweep, "hybrid": bench_hybrid,
           "decode-positions": bench_decode_positions, "chunked": bench_chunked,
-          "paged-decode": bench_paged_decode}[args.workload]
+          "paged-decode": bench_paged_decode, "backward": bench_backward}[args.workload]
     for line in fn(swa, device, stream, peaks):
         line["peak_source"] = peaks["source"]
         print(json.dumps(line), flush=True)
@@ -804,7 +840,7 @@ def main(argv=None):
     ap.add_argument("--skip-llama", action="store_true", help="omit the Llama-shaped layer loop")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer measurement")
     ap.add_argument("--workload", choices=("step", "window-sweep", "hybrid", "decode-positions",
-                                           "chunked", "paged-decode"),
+                                           "chunked", "paged-decode", "backward"),
                     default="step", help="step (default): the benchmark line; the others print "
                     "supplementary lines for the other configurations (1 GPU)")
     args = ap.parse_args(argv)

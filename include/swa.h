@@ -71,6 +71,39 @@ SWA_API int swa_prefill(const void *q, const void *k, const void *v, void *out,
                 int B, int L, int Hq, int Hkv, int d, int w, int s,
                 float scale, swa_stream_t stream);
 
+/* Prefill that also writes each row's log-sum-exp of its scaled scores,
+ *   lse[b, hq, t] = log(sum_{j in K(t)} exp(scale * q_t . k_j))   (natural log),
+ * as fp32 [B, Hq, L] (4-byte aligned): what swa_prefill_backward needs to
+ * recompute the softmax weights. Otherwise identical to swa_prefill. */
+SWA_API int swa_prefill_lse(const void *q, const void *k, const void *v, void *out, float *lse,
+                            int B, int L, int Hq, int Hkv, int d, int w, int s, float scale,
+                            swa_stream_t stream);
+
+/* Backward of the prefill: the gradients of the outputs with respect to q, k
+ * and v for an upstream gradient dout. The pages give no backward formulas;
+ * they mention SWA-aware fine-tuning (the SWAA page, "如何将Sliding Window
+ * Attention Adaptation应用到你的LLM项目中", section "微调：提升SWAA适应性"). This
+ * is the chain rule applied to the forward definition above: for every row
+ * (b, hq, t) and key j in K(t), with P the forward's softmax weights,
+ *   dP_tj = dout_t . v_j,  D_t = dout_t . out_t,  dS_tj = P_tj (dP_tj - D_t),
+ *   dq_t = scale sum_j dS_tj k_j,  dk_j = scale sum_t dS_tj q_t,
+ *   dv_j = sum_t P_tj dout_t,
+ * with dk and dv summed over the query heads of each KV head group.
+ *   q, out, dout [B, L, Hq, d] bf16; k, v [B, L, Hkv, d] bf16 (the forward's
+ *   inputs and output); lse fp32 [B, Hq, L] from swa_prefill_lse on the same
+ *   inputs; dq [B, L, Hq, d], dk, dv [B, L, Hkv, d] bf16 (written in full).
+ *   workspace: caller-owned device memory of at least
+ *   swa_prefill_backward_workspace_size(...) bytes, 16-byte aligned.
+ * Only the key tiles inside each query block's window (plus the sinks) are
+ * visited, as in the forward pass. Products run on the tensor cores with fp32
+ * accumulation; P and dS are rounded to bf16 before their products; the
+ * gradients are rounded to bf16. */
+SWA_API size_t swa_prefill_backward_workspace_size(int B, int L, int Hq, int Hkv, int d, int s);
+SWA_API int swa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
+                                 const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                 int B, int L, int Hq, int Hkv, int d, int w, int s, float scale,
+                                 void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
 /* Ring-cache append: store T consecutive new tokens of every sequence.
  *   k_new, v_new [B, T, Hkv, d] bf16     kcache, vcache [B, Hkv, s + w, d] bf16
  *   pos_start    DEVICE int32[B]: position of token 0 of this call, per sequence

@@ -42,6 +42,13 @@ _sz = ctypes.c_size_t
 
 _lib.swa_prefill.restype = _i
 _lib.swa_prefill.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.swa_prefill_lse.restype = _i
+_lib.swa_prefill_lse.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.swa_prefill_backward_workspace_size.restype = _sz
+_lib.swa_prefill_backward_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+_lib.swa_prefill_backward.restype = _i
+_lib.swa_prefill_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                      _i, _i, _i, _f, _vp, _sz, _vp]
 _lib.swa_cache_append.restype = _i
 _lib.swa_cache_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]
 _lib.swa_decode_workspace_size.restype = _sz
@@ -173,12 +180,15 @@ def _default_scale(d: int, scale):
 # ---------------------------------------------------------------- prefill
 
 def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
-                scale: float | None = None, out: torch.Tensor | None = None, stream=None):
+                scale: float | None = None, out: torch.Tensor | None = None, stream=None,
+                lse: torch.Tensor | None = None):
     """SWA(w, s) prefill. q [B,L,Hq,d], k/v [B,L,Hkv,d] bf16 -> out [B,L,Hq,d].
 
     CUDA tensors run asynchronously on the current stream. CPU tensors are the
     host-buffer path: they are copied to the current device, the kernel runs,
     and the result is copied back to a (pinned) host tensor before returning.
+    lse (CUDA fp32 [B, Hq, L], optional) also receives each row's log-sum-exp
+    (swa_prefill_lse), which swa_prefill_backward needs.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _ndim(t, 4, n)
@@ -186,7 +196,13 @@ def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: in
     if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     _expect_shape(out, q.shape, "out")
+    if lse is not None:
+        _expect_shape(lse, (B, Hq, L), "lse")
+        if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+            raise TypeError("lse must be a contiguous CUDA float32 tensor")
     if not q.is_cuda:
+        if lse is not None:
+            raise ValueError("lse is supported with CUDA tensors only")
         dev = torch.device("cuda", torch.cuda.current_device())
         qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
         od = swa_prefill(qd, kd, vd, w, s, scale, None, stream)
@@ -201,9 +217,55 @@ def swa_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: in
         out = torch.empty_like(q)
     else:
         _bf16_cuda(out, "out")
+    if lse is not None:
+        _check(_lib.swa_prefill_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, Hq,
+                                    Hkv, d, int(w), int(s), _default_scale(d, scale),
+                                    _stream(stream)), "swa_prefill_lse")
+        return out
     _check(_lib.swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, L, Hq, Hkv, d, int(w),
                             int(s), _default_scale(d, scale), _stream(stream)), "swa_prefill")
     return out
+
+
+def swa_prefill_backward_workspace_size(B: int, L: int, Hq: int, Hkv: int, d: int, s: int) -> int:
+    return int(_lib.swa_prefill_backward_workspace_size(B, L, Hq, Hkv, d, s))
+
+
+def swa_prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                         dout: torch.Tensor, lse: torch.Tensor, w: int, s: int,
+                         scale: float | None = None, dq=None, dk=None, dv=None, workspace=None,
+                         stream=None):
+    """Gradients (dq [B,L,Hq,d], dk, dv [B,L,Hkv,d], bf16) of the SWA(w, s)
+    prefill for the upstream gradient dout [B,L,Hq,d]; out and lse are the
+    forward's output and row log-sum-exp (swa_prefill(..., lse=...))."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _ndim(t, 4, n)
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, L, Hkv, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    _expect_shape(out, q.shape, "out")
+    _expect_shape(dout, q.shape, "dout")
+    _expect_shape(lse, (B, Hq, L), "lse")
+    _expect_shape(dq, q.shape, "dq")
+    _expect_shape(dk, k.shape, "dk")
+    _expect_shape(dv, k.shape, "dv")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _bf16_cuda(t, n)
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise TypeError("lse must be a contiguous CUDA float32 tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = swa_prefill_backward_workspace_size(B, L, Hq, Hkv, d, s)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.swa_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, L, Hq, Hkv, d, int(w),
+                                     int(s), _default_scale(d, scale), _ptr(workspace), wbytes,
+                                     _stream(stream)), "swa_prefill_backward")
+    return dq, dk, dv
 
 
 prefill = swa_prefill

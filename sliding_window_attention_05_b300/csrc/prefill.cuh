@@ -55,6 +55,7 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max 
 
 struct PrefillArgs {
   __nv_bfloat16 *out;
+  float *lse;         // [B, Hq, L] log-sum-exp of each row's scores (natural log), or null
   int B, L, Hq, Hkv, w, s;
   float scale_log2;   // scale * log2(e)
   PrefillPlan plan;
@@ -608,6 +609,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       xl[half * 128 + r] = l_part;
       named_bar_sync(bar_id, 64);
       const float l_sum = l_part + xl[(half ^ 1) * 128 + r];
+      if (a.lse != nullptr && half == 0 && r < plan.rows && t < a.L) {
+        // m_used is in log2 units of the scaled scores
+        const int hq = (wk.bh() % a.Hkv) * plan.G + r % plan.G;
+        a.lse[((size_t)(wk.bh() / a.Hkv) * a.Hq + hq) * a.L + t] =
+            (m_used + log2f(l_sum)) * 0.6931471805599453f;
+      }
       if (!warp_wait(o_full, it & 1)) { ok = false; break; }
       // a separate staging buffer is free once the previous block's store read it
       if (a.sep_stage && !warp_wait(stage_free, (it & 1) ^ 1)) { ok = false; break; }

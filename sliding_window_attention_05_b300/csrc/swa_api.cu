@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "../../include/swa.h"
+#include "backward.cuh"
 #include "chunk.cuh"
 #include "decode.cuh"
 #include "page_pool.h"
@@ -176,7 +177,7 @@ size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages, bool 
 template <int D>
 int launch_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
                    int Hkv, int w, int s, float scale, cudaStream_t stream,
-                   const DeviceInfo &dev, int qb_first = 0) {
+                   const DeviceInfo &dev, int qb_first = 0, float *lse = nullptr) {
   const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
   CUtensorMap tq, tk, tv, tks, tvs, to;
   int rc;
@@ -201,6 +202,7 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
 
   swa::PrefillArgs a;
   a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  a.lse = lse;
   a.B = B;
   a.L = L;
   a.Hq = Hq;
@@ -413,6 +415,126 @@ ChunkWorkspace chunk_workspace(int B, int T, int Hq, int Hkv, int d, int w, int 
   return c;
 }
 
+// Device workspace of swa_prefill_backward: D = dO . O per row (fp32
+// [B, Hq, L]), then the sink keys' fp32 dK and dV accumulators ([B, Hkv,
+// s_eff, d] each).
+struct BwdWorkspace {
+  size_t D, sink_dk, sink_dv, total;
+};
+
+BwdWorkspace bwd_workspace(int B, int L, int Hq, int Hkv, int d, int s) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t s_eff = (size_t)(s < L ? s : L);
+  BwdWorkspace w;
+  w.D = 0;
+  w.sink_dk = up((size_t)B * Hq * L * sizeof(float));
+  w.sink_dv = w.sink_dk + up((size_t)B * Hkv * s_eff * d * sizeof(float));
+  w.total = w.sink_dv + up((size_t)B * Hkv * s_eff * d * sizeof(float));
+  return w;
+}
+
+template <int D>
+int launch_backward(const void *q, const void *k, const void *v, const void *out,
+                    const void *dout, const float *lse, void *dq, void *dk, void *dv, int B, int L,
+                    int Hq, int Hkv, int w, int s, float scale, void *workspace,
+                    cudaStream_t stream, const DeviceInfo &dev) {
+  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  const BwdWorkspace ws = bwd_workspace(B, L, Hq, Hkv, D, s);
+  uint8_t *base = reinterpret_cast<uint8_t *>(workspace);
+  swa::BwdArgs a;
+  a.out = reinterpret_cast<const __nv_bfloat16 *>(out);
+  a.dout = reinterpret_cast<const __nv_bfloat16 *>(dout);
+  a.lse = lse;
+  a.D = reinterpret_cast<float *>(base + ws.D);
+  a.sink_dk = reinterpret_cast<float *>(base + ws.sink_dk);
+  a.sink_dv = reinterpret_cast<float *>(base + ws.sink_dv);
+  a.dq = reinterpret_cast<__nv_bfloat16 *>(dq);
+  a.dk = reinterpret_cast<__nv_bfloat16 *>(dk);
+  a.dv = reinterpret_cast<__nv_bfloat16 *>(dv);
+  a.B = B;
+  a.L = L;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.w = w;
+  a.s = s;
+  a.s_eff = s < L ? s : L;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.plan = plan;
+  a.n_band_tiles = L > s ? swa::cdiv(L - s, 128) : 0;
+  a.n_sink_items = a.s_eff > 0 ? swa::cdiv(a.s_eff, 128) * swa::cdiv(plan.nqb, swa::kBwdSinkChunk) : 0;
+
+  // 1. D = dO . O, sink accumulators cleared
+  const long long n_rows = (long long)B * L * Hq;
+  const long long n_sink = (long long)B * Hkv * a.s_eff * D;
+  long long blocks = (n_rows * 32 + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "backward too large");
+  cudaError_t e = launch_pdl(swa::swa_bwd_pre_kernel<D>, dim3((unsigned)blocks), dim3(256), 0,
+                             stream, a, n_rows, n_sink);
+  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_backward pre launch");
+
+  // 2. dQ: one query block per work item, the forward's tiles
+  {
+    CUtensorMap tq, tdo, tk, tv, tks, tvs;
+    int rc;
+    if ((rc = make_map_bf16_4d(&tq, q, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+    if ((rc = make_map_bf16_4d(&tdo, dout, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+    if ((rc = make_map_bf16_4d(&tk, k, B, L, Hkv, D, 1, plan.n_band))) return rc;
+    if ((rc = make_map_bf16_4d(&tv, v, B, L, Hkv, D, 1, plan.n_band))) return rc;
+    if (plan.n_sink > 0) {
+      if ((rc = make_map_bf16_4d(&tks, k, B, L, Hkv, D, 1, plan.s_box))) return rc;
+      if ((rc = make_map_bf16_4d(&tvs, v, B, L, Hkv, D, 1, plan.s_box))) return rc;
+    } else {
+      tks = tk;
+      tvs = tv;
+    }
+    const int stages = swa::BwdDqSmem<D>::stages(plan, dev.max_smem_optin);
+    if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the dQ pipeline");
+    const size_t smem = swa::BwdDqSmem<D>::bytes(plan, stages);
+    const cudaError_t attr = ensure_max_dynamic_smem(
+        reinterpret_cast<const void *>(swa::swa_bwd_dq_kernel<D>), dev.max_smem_optin);
+    if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(backward dQ)");
+    swa::BwdArgs ad = a;
+    ad.n_items = B * Hkv * plan.nqb;
+    ad.stages = stages;
+    ad.kv_chunk = plan.slot_keys * 128;
+    const int grid = swa::imin(ad.n_items, dev.sms);
+    e = launch_pdl(swa::swa_bwd_dq_kernel<D>, dim3(grid), dim3(swa::kPrefillThreads), smem, stream,
+                   tq, tdo, tk, tv, tks, tvs, ad);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_backward dQ launch");
+  }
+  // 3. dK, dV: one key tile per CTA
+  {
+    CUtensorMap tq, tdo, tkt, tvt;
+    int rc;
+    if ((rc = make_map_bf16_4d(&tq, q, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+    if ((rc = make_map_bf16_4d(&tdo, dout, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+    if ((rc = make_map_bf16_4d(&tkt, k, B, L, Hkv, D, 1, 128))) return rc;
+    if ((rc = make_map_bf16_4d(&tvt, v, B, L, Hkv, D, 1, 128))) return rc;
+    const size_t smem = swa::BwdDkvSmem<D>::bytes();
+    const cudaError_t attr = ensure_max_dynamic_smem(
+        reinterpret_cast<const void *>(swa::swa_bwd_dkv_kernel<D>), (int)smem);
+    if (attr != cudaSuccess) return cuda_fail(attr, "cudaFuncSetAttribute(backward dK dV)");
+    const long long items = (long long)B * Hkv * (a.n_band_tiles + a.n_sink_items);
+    if (items > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "too many key tiles");
+    if (items > 0) {
+      e = launch_pdl(swa::swa_bwd_dkv_kernel<D>, dim3((unsigned)items), dim3(swa::kPrefillThreads),
+                     smem, stream, tq, tdo, tkt, tvt, a);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_backward dK/dV launch");
+    }
+  }
+  // 4. the sink keys' rows of dK and dV
+  if (n_sink > 0) {
+    e = launch_pdl(swa::swa_bwd_sink_out_kernel, dim3((unsigned)((n_sink + 255) / 256)),
+                   dim3(256), 0, stream, a, D);
+    if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_backward sink launch");
+  }
+  return SWA_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -490,6 +612,70 @@ int swa_prefill(const void *q, const void *k, const void *v, void *out, int B, i
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (d == 64) return launch_prefill<64>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev);
   return launch_prefill<128>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev);
+}
+
+int swa_prefill_lse(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                    int L, int Hq, int Hkv, int d, int w, int s, float scale,
+                    swa_stream_t stream) {
+  if (!lse) return fail(SWA_ERR_INVALID_ARG, "lse is NULL");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(SWA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!q || !k || !v || !out) return fail(SWA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(SWA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || L < 1) return fail(SWA_ERR_INVALID_ARG, "B and L must be >= 1");
+  if (w < 1) return fail(SWA_ERR_INVALID_ARG, "window w must be >= 1");
+  if (s < 0) return fail(SWA_ERR_INVALID_ARG, "sink count s must be >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if ((rc = check_scale(scale))) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if ((long long)B * Hkv * swa::cdiv(L, 128 / (Hq / Hkv)) > 0x7FFFFFFFll)
+    return fail(SWA_ERR_UNSUPPORTED, "too many query blocks");
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64) return launch_prefill<64>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev, 0, lse);
+  return launch_prefill<128>(q, k, v, out, B, L, Hq, Hkv, w, s, scale, st, dev, 0, lse);
+}
+
+size_t swa_prefill_backward_workspace_size(int B, int L, int Hq, int Hkv, int d, int s) {
+  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || s < 0 || !supported_d(d)) return 0;
+  return bwd_workspace(B, L, Hq, Hkv, d, s).total;
+}
+
+int swa_prefill_backward(const void *q, const void *k, const void *v, const void *out,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                         int L, int Hq, int Hkv, int d, int w, int s, float scale,
+                         void *workspace, size_t workspace_bytes, swa_stream_t stream) {
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
+    return fail(SWA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(SWA_ERR_INVALID_ARG, "pointers must be 16-byte aligned (lse 4-byte)");
+  if (B < 1 || L < 1) return fail(SWA_ERR_INVALID_ARG, "B and L must be >= 1");
+  if (w < 1) return fail(SWA_ERR_INVALID_ARG, "window w must be >= 1");
+  if (s < 0) return fail(SWA_ERR_INVALID_ARG, "sink count s must be >= 0");
+  int rc = check_heads(Hq, Hkv);
+  if (rc) return rc;
+  if ((rc = check_scale(scale))) return rc;
+  if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
+  if (B > 65535) return fail(SWA_ERR_UNSUPPORTED, "B > 65535");
+  if ((long long)B * Hkv * swa::cdiv(L, 128 / (Hq / Hkv)) > 0x7FFFFFFFll)
+    return fail(SWA_ERR_UNSUPPORTED, "too many query blocks");
+  const size_t need = bwd_workspace(B, L, Hq, Hkv, d, s).total;
+  if (!workspace || workspace_bytes < need)
+    return fail(SWA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace ? workspace_bytes : (size_t)0, need);
+  DeviceInfo dev;
+  if ((rc = current_device_info(&dev))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return launch_backward<64>(q, k, v, out, dout, lse, dq, dk, dv, B, L, Hq, Hkv, w, s, scale,
+                               workspace, st, dev);
+  return launch_backward<128>(q, k, v, out, dout, lse, dq, dk, dv, B, L, Hq, Hkv, w, s, scale,
+                              workspace, st, dev);
 }
 
 int swa_cache_append(const void *k_new, const void *v_new, void *kcache, void *vcache,
