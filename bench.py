@@ -604,6 +604,27 @@ def bench_chunked(swa, device, stream, peaks, iters=5):
                       "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
                       "tensor_frac": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                       "vs_one_call": round(one / ms, 3)})
+    # the same prompt into the paged layout (pages of 64 positions); the
+    # host-side page reservation and table copy of every chunk are timed too
+    T, P = 1024, 64
+    with torch.cuda.stream(stream):
+        pool = swa.PagePool(B * (L // P + 2), Hkv, d, page_size=P, device=device)
+        pcache = swa.PagedKVCache(pool, B, w, s, max_len=L)
+        chunks = [(q[:, p:p + T].contiguous(), k[:, p:p + T].contiguous(),
+                   v[:, p:p + T].contiguous(), out[:, p:p + T].contiguous())
+                  for p in range(0, L, T)]
+
+    def run_paged():
+        pcache.release()
+        for qc, kc, vc, oc in chunks:
+            pcache.prefill_chunk(qc, kc, vc, out=oc, stream=stream)
+
+    ms = _time_events(run_paged, stream, iters)
+    lines.append({"workload": f"paged chunked prefill SWA({w},{s}) B={B} L={L} in chunks of {T},"
+                              f" pages of {P}",
+                  "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                  "tensor_frac": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                  "vs_one_call": round(one / ms, 3)})
     return lines
 
 

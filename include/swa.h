@@ -132,11 +132,11 @@ SWA_API int swa_cache_append(const void *k_new, const void *v_new, void *kcache,
  *   positions, which the ring keeps.
  *   workspace: caller-owned device memory of at least
  *   swa_prefill_chunk_workspace_size(...) bytes, 16-byte aligned; its size grows
- *   with (min(pos0, s + w - 1) + T) rows of q, k, v and out.
- * The work: a staging kernel lays the kept cache rows and the chunk out
- * contiguously in the workspace, the prefill kernel runs over the query blocks
- * that hold chunk rows, a copy kernel writes the chunk's rows to out, and the
- * append kernel stores the chunk. */
+ *   with (min(pos0, s + w - 1) + T) rows of k and v.
+ * The work: a staging kernel lays out the kept cache rows of k and v, then
+ * the chunk's, contiguously in the workspace, the prefill kernel runs over the
+ * query blocks that hold chunk rows, reading q and writing out in place, and
+ * the append kernel stores the chunk. */
 SWA_API size_t swa_prefill_chunk_workspace_size(int B, int T, int Hq, int Hkv, int d, int w, int s,
                                                 long long pos0);
 SWA_API int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kcache,
@@ -231,6 +231,16 @@ SWA_API int swa_page_pool_free_pages(swa_page_pool *pool);
  * Thread-safe per pool; the table is the caller's. */
 SWA_API int swa_paged_reserve(swa_page_pool *pool, int *table, int max_pages, long long pos_hi,
                               int w, int s, int page_size);
+/* swa_paged_reserve for a run of positions: the table then maps the pages of
+ * every K(p) with pos_lo <= p <= pos_hi (the sink pages and the pages of
+ * positions pos_lo - w + 1 .. pos_hi), which a chunk of prompt tokens at
+ * pos_lo .. pos_hi reads and writes; other mapped pages are returned.
+ * swa_paged_reserve(..., pos_hi, ...) is this call with pos_lo = pos_hi. Call it
+ * with non-decreasing pos_lo. Same errors as swa_paged_reserve, plus
+ * SWA_ERR_INVALID_ARG for pos_lo > pos_hi. */
+SWA_API int swa_paged_reserve_range(swa_page_pool *pool, int *table, int max_pages,
+                                    long long pos_lo, long long pos_hi, int w, int s,
+                                    int page_size);
 /* Return every page of a table to the pool and unmap it (end of a sequence). */
 SWA_API int swa_paged_release(swa_page_pool *pool, int *table, int max_pages);
 
@@ -251,6 +261,26 @@ SWA_API int swa_paged_decode(const void *q, const void *kpool, const void *vpool
                              int Hkv, int d, int page_size, int max_pages, int n_pages, int w,
                              int s, float scale, void *workspace, size_t workspace_bytes,
                              swa_stream_t stream);
+
+/* Paged swa_prefill_chunk: the chunk of T prompt tokens at positions
+ * pos0 .. pos0 + T - 1 attends over the keys the pages still hold plus its
+ * own, and is then appended to the pages (a long prompt prefilled in pieces,
+ * wiblog.cn long-context SWA article, section "长 Prompt 的分块处理与工程实现",
+ * into the paged hybrid layout of "Hybrid Sliding Window Attention (Hybrid
+ * SWA)", section "三、1. vLLM 中的 Hybrid KV Cache 最佳实践").
+ *   q, k_new, v_new, out as swa_prefill_chunk; kpool, vpool and n_pages as
+ *   swa_paged_append; page_table DEVICE int32 [B, max_pages], prepared by
+ *   swa_paged_reserve_range(pos0, pos0 + T - 1) so that every page the chunk
+ *   reads or writes is mapped; every position < pos0 must already have been
+ *   appended. workspace: swa_prefill_chunk_workspace_size(...) bytes.
+ * A prefix row on an unmapped page is read as zeros and flagged in the device
+ * error word; the append skips and flags unmapped pages as swa_paged_append. */
+SWA_API int swa_paged_prefill_chunk(const void *q, const void *k_new, const void *v_new,
+                                    void *kpool, void *vpool, const int *page_table, void *out,
+                                    int B, int T, int Hq, int Hkv, int d, int page_size,
+                                    int max_pages, int n_pages, int w, int s, long long pos0,
+                                    float scale, void *workspace, size_t workspace_bytes,
+                                    swa_stream_t stream);
 
 /* Host helper: the cache slot of position pos (the formula above), or -1 for
  * pos < 0, w < 1 or s < 0. */

@@ -71,6 +71,12 @@ _lib.swa_page_pool_free_pages.restype = _i
 _lib.swa_page_pool_free_pages.argtypes = [_vp]
 _lib.swa_paged_reserve.restype = _i
 _lib.swa_paged_reserve.argtypes = [_vp, _vp, _i, ctypes.c_longlong, _i, _i, _i]
+_lib.swa_paged_reserve_range.restype = _i
+_lib.swa_paged_reserve_range.argtypes = [_vp, _vp, _i, ctypes.c_longlong, ctypes.c_longlong, _i,
+                                         _i, _i]
+_lib.swa_paged_prefill_chunk.restype = _i
+_lib.swa_paged_prefill_chunk.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                         _i, _i, _i, _i, ctypes.c_longlong, _f, _vp, _sz, _vp]
 _lib.swa_paged_release.restype = _i
 _lib.swa_paged_release.argtypes = [_vp, _vp, _i]
 _lib.swa_paged_append.restype = _i
@@ -492,11 +498,18 @@ class PagePool:
     def free_pages(self) -> int:
         return int(_lib.swa_page_pool_free_pages(self._h))
 
-    def reserve(self, table, pos_hi: int, w: int, s: int):
-        """table: host int32 tensor [max_pages] (contiguous)."""
-        _check(_lib.swa_paged_reserve(self._h, ctypes.c_void_p(table.data_ptr()), table.numel(),
-                                      int(pos_hi), int(w), int(s), self.page_size),
-               "swa_paged_reserve")
+    def reserve(self, table, pos_hi: int, w: int, s: int, pos_lo: int | None = None):
+        """table: host int32 tensor [max_pages] (contiguous). Maps the pages of
+        K(p) for every p in [pos_lo, pos_hi] (pos_lo defaults to pos_hi)."""
+        if pos_lo is None:
+            _check(_lib.swa_paged_reserve(self._h, ctypes.c_void_p(table.data_ptr()),
+                                          table.numel(), int(pos_hi), int(w), int(s),
+                                          self.page_size), "swa_paged_reserve")
+        else:
+            _check(_lib.swa_paged_reserve_range(self._h, ctypes.c_void_p(table.data_ptr()),
+                                                table.numel(), int(pos_lo), int(pos_hi), int(w),
+                                                int(s), self.page_size),
+                   "swa_paged_reserve_range")
 
     def release(self, table):
         _check(_lib.swa_paged_release(self._h, ctypes.c_void_p(table.data_ptr()), table.numel()),
@@ -528,15 +541,16 @@ class PagedKVCache:
         self.pos_dev = torch.zeros(B, dtype=torch.int32, device=device)
         self._pos_value = 0          # what pos_dev holds (set only when it changes)
         self._workspace = None
+        self._chunk_ws = None
 
     def _set_pos(self, value: int):
         if value != self._pos_value:
             self.pos_dev.fill_(value)
             self._pos_value = value
 
-    def _reserve(self, pos_hi: int):
+    def _reserve(self, pos_hi: int, pos_lo: int | None = None):
         for b in range(self.B):
-            self.pool.reserve(self.table[b], pos_hi, self.w, self.s)
+            self.pool.reserve(self.table[b], pos_hi, self.w, self.s, pos_lo)
         self.table_dev.copy_(self.table)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
@@ -551,6 +565,34 @@ class PagedKVCache:
                                      self.pool.page_size, self.max_pages, self.pool.n_pages,
                                      self.w, self.s, _stream(stream)), "swa_paged_append")
         self.length += T
+
+    def prefill_chunk(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      scale: float | None = None, out=None, stream=None):
+        """Attention of the next T prompt tokens (q [B,T,Hq,d], k_new/v_new
+        [B,T,Hkv,d]) over the pages plus themselves; the chunk is then appended."""
+        _ndim(q, 4, "q")
+        B, T, Hq, d = q.shape
+        Hkv = self.pool.Hkv
+        _expect_shape(k_new, (self.B, T, Hkv, self.pool.d), "k_new")
+        _expect_shape(v_new, (self.B, T, Hkv, self.pool.d), "v_new")
+        _expect_shape(out, q.shape, "out")
+        for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
+            _bf16_cuda(t, n)
+        if out is None:
+            out = torch.empty_like(q)
+        pos0 = self.length
+        self._reserve(pos0 + T - 1, pos0)
+        need = swa_prefill_chunk_workspace_size(B, T, Hq, Hkv, d, self.w, self.s, pos0)
+        if self._chunk_ws is None or self._chunk_ws.numel() < need:
+            self._chunk_ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        _check(_lib.swa_paged_prefill_chunk(
+            _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(self.pool.k), _ptr(self.pool.v),
+            _ptr(self.table_dev), _ptr(out), B, T, Hq, Hkv, d, self.pool.page_size,
+            self.max_pages, self.pool.n_pages, self.w, self.s, pos0, _default_scale(d, scale),
+            _ptr(self._chunk_ws), self._chunk_ws.numel(), _stream(stream)),
+            "swa_paged_prefill_chunk")
+        self.length += T
+        return out
 
     def decode(self, q: torch.Tensor, scale: float | None = None, out=None, stream=None):
         """q [B, Hq, d]: attend at the newest position (length - 1)."""

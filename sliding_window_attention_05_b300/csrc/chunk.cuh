@@ -8,15 +8,18 @@
 // the ring cache holds exactly those once every position < pos0 has been
 // appended (and, while pos0 <= s + w - 1, every position < pos0).
 //
-// The chunk runs through the prefill kernel on a contiguous staging copy
-// whose row index differs from the position by a constant over the window
-// part, so the kernel's band, causal and sink rules carry over unchanged:
+// The chunk runs through the prefill kernel on a contiguous staging copy of
+// the keys and values whose row index differs from the position by a
+// constant over the window part, so the kernel's band, causal and sink rules
+// carry over unchanged:
 //   pos0 <= s + w - 1: rows 0 .. pos0 - 1 are positions 0 .. pos0 - 1;
 //   otherwise:         rows 0 .. s - 1 are the sinks, rows s .. s + w - 2 are
 //                      positions pos0 - w + 1 .. pos0 - 1;
-// then the T chunk rows. Query blocks made only of prefix rows are not
-// computed; the prefix rows of the first computed block get zero queries
-// (finite scores) and their outputs are not used.
+// then the T chunk rows. The queries stay in the caller's q: the kernel reads
+// staged row n_pre + i from row i of q and writes it to row i of out. Query
+// blocks made only of prefix rows are not computed; the prefix rows of the
+// first computed block read zero queries (the TMA fill value below row 0 of
+// q: finite scores) and their outputs are not stored.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -39,24 +42,31 @@ SWA_HD long long chunk_prefix_pos(long long r, long long pos0, int w, int s) {
   return pos0 - w + 1 + (r - s);
 }
 
-// Stage [prefix | chunk] rows: qx [B, Lx, Hq, d], kx/vx [B, Lx, Hkv, d] with
-// Lx = n_pre + T; query rows below q_row0 (blocks the prefill skips) are not
-// written. One thread moves 16 bytes of one (b, row, head) of the Hq + 2 Hkv
-// heads. Thread 0 also writes pos0 into pos_out[B] for the append
-// that follows.
-__global__ void swa_chunk_stage_kernel(const uint4 *__restrict__ q, const uint4 *__restrict__ k_new,
-                                       const uint4 *__restrict__ v_new,
-                                       const uint4 *__restrict__ kcache,
-                                       const uint4 *__restrict__ vcache, uint4 *__restrict__ qx,
+// Where the staging reads the kept cache rows from: a ring cache
+// [B, Hkv, s + w, d] (table == nullptr) or the pages of a paged pool
+// [n_pages, Hkv, page_size, d] through a page table [B, max_pages].
+struct ChunkSource {
+  const uint4 *kcache, *vcache;
+  const int *table;
+  int page_size, max_pages, n_pages;
+};
+
+// Stage the key/value rows [prefix | chunk] into kx, vx [B, Lx, Hkv, d] with
+// Lx = n_pre + T. The queries and outputs are not staged: the prefill kernel
+// reads q and writes out at row (staged row - n_pre). One thread moves 16
+// bytes of one (b, row, K or V head). Thread 0 of sequence 0 also writes pos0
+// into pos_out[B] for the append that follows. A prefix row whose page is
+// unmapped is staged as zeros and flagged in the device error word.
+__global__ void swa_chunk_stage_kernel(const uint4 *__restrict__ k_new,
+                                       const uint4 *__restrict__ v_new, const ChunkSource src,
                                        uint4 *__restrict__ kx, uint4 *__restrict__ vx,
-                                       int *__restrict__ pos_out, int B, int T, int Hq, int Hkv,
-                                       int d, int w, int s, long long pos0, int n_pre,
-                                       int q_row0) {
+                                       int *__restrict__ pos_out, int B, int T, int Hkv, int d,
+                                       int w, int s, long long pos0, int n_pre) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int b = blockIdx.y;
   const int vpr = d / 8;                    // 16-byte units per row of one head
-  const int heads = Hq + 2 * Hkv;
+  const int heads = 2 * Hkv;                // K heads, then V heads
   const long long Lx = (long long)n_pre + T;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (b == 0 && idx < B) pos_out[idx] = (int)pos0;
@@ -64,41 +74,31 @@ __global__ void swa_chunk_stage_kernel(const uint4 *__restrict__ q, const uint4 
   const int c = (int)(idx % vpr);
   const int h = (int)((idx / vpr) % heads);
   const long long r = idx / ((long long)vpr * heads);
-  if (h < Hq) {  // query rows (those below q_row0 are never read)
-    if (r < q_row0) return;
-    const long long dst = (((long long)b * Lx + r) * Hq + h) * vpr + c;
-    if (r < n_pre)
-      qx[dst] = make_uint4(0, 0, 0, 0);
-    else
-      qx[dst] = q[(((long long)b * T + (r - n_pre)) * Hq + h) * vpr + c];
-    return;
-  }
-  const bool is_v = h >= Hq + Hkv;
-  const int kvh = h - Hq - (is_v ? Hkv : 0);
+  const bool is_v = h >= Hkv;
+  const int kvh = is_v ? h - Hkv : h;
   const long long dst = (((long long)b * Lx + r) * Hkv + kvh) * vpr + c;
-  uint4 val;
+  uint4 val = make_uint4(0, 0, 0, 0);
   if (r < n_pre) {
-    const long long slot = ring_slot(chunk_prefix_pos(r, pos0, w, s), w, s);
-    const long long src = (((long long)b * Hkv + kvh) * (s + w) + slot) * vpr + c;
-    val = is_v ? vcache[src] : kcache[src];
+    const long long p = chunk_prefix_pos(r, pos0, w, s);
+    long long at;
+    if (src.table == nullptr) {
+      at = (((long long)b * Hkv + kvh) * (s + w) + ring_slot(p, w, s)) * vpr + c;
+    } else {
+      const long long lp = p / src.page_size;
+      const int page = lp < src.max_pages ? src.table[(long long)b * src.max_pages + lp] : -1;
+      if (page < 0 || page >= src.n_pages) {
+        record_error(kErrMissingPage);
+        at = -1;
+      } else {
+        at = (((long long)page * Hkv + kvh) * src.page_size + p % src.page_size) * vpr + c;
+      }
+    }
+    if (at >= 0) val = is_v ? src.vcache[at] : src.kcache[at];
   } else {
-    const long long src = (((long long)b * T + (r - n_pre)) * Hkv + kvh) * vpr + c;
-    val = is_v ? v_new[src] : k_new[src];
+    const long long at = (((long long)b * T + (r - n_pre)) * Hkv + kvh) * vpr + c;
+    val = is_v ? v_new[at] : k_new[at];
   }
   (is_v ? vx : kx)[dst] = val;
-}
-
-// out[b, i] = ox[b, n_pre + i] for the T chunk rows (16 bytes per thread).
-__global__ void swa_chunk_out_kernel(const uint4 *__restrict__ ox, uint4 *__restrict__ out, int T,
-                                     int Hq, int d, int n_pre) {
-  grid_launch_dependents();
-  grid_dependency_wait();
-  const int b = blockIdx.y;
-  const long long row_units = (long long)Hq * (d / 8);
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)T * row_units) return;
-  const long long Lx = (long long)n_pre + T;
-  out[(long long)b * T * row_units + idx] = ox[((long long)b * Lx + n_pre) * row_units + idx];
 }
 
 }  // namespace swa

@@ -57,6 +57,9 @@ struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;         // [B, Hq, L] log-sum-exp of each row's scores (natural log), or null
   int B, L, Hq, Hkv, w, s;
+  int q_off;          // K/V rows before row 0 of q and out: query row t of the
+                      // key/value layout is row t - q_off of q and out, which
+                      // hold L - q_off rows (0 for a whole prompt)
   float scale_log2;   // scale * log2(e)
   PrefillPlan plan;
   int n_items;
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)(kChunks * 64 * plan.rows * 2));
             for (int c = 0; c < kChunks; ++c)
               tma_load_4d(sQ + qbuf * kQBytes + c * kChunkBytes, &tm_q, &q_full[qbuf], c * 64,
-                          kvh * plan.G, bt.t0, b, pol_q);
+                          kvh * plan.G, bt.t0 - a.q_off, b, pol_q);
             ++q_issued;
           }
         }
@@ -494,26 +497,53 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ output store
     // The softmax warps stage each finished block, bf16, in the Q buffer it
-    // was computed from (same swizzled layout as the Q tile). This thread
-    // stores it with TMA and then frees the buffer for the next Q load.
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_o);
-      int it = 0;
-      for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); wk.valid();
-           wk.next(), ++it) {
-        const int qb = wk.qb();
-        const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
-        const int qbuf = it & 1;
-        if (!mbar_wait(epi_staged, it & 1, abort_flag)) break;
-        const uint8_t *src = a.sep_stage ? sStage : sQ + qbuf * kQBytes;
-        for (int c = 0; c < kChunks; ++c)
-          tma_store_4d(&tm_o, src + c * kChunkBytes, c * 64, kvh * plan.G, qb * plan.Tq, b);
-        tma_store_commit();
-        tma_store_wait_read();
-        mbar_arrive(a.sep_stage ? stage_free : &q_empty[qbuf]);
+    // was computed from (same swizzled layout as the Q tile). Lane 0 stores it
+    // with TMA and then frees the buffer for the next Q load. A block that
+    // starts before row 0 of out (q_off > 0: its first rows are K/V rows that
+    // have no query) is copied by the whole warp with plain stores instead,
+    // row by row from row 0 of out on, since a TMA store may not start at a
+    // negative coordinate.
+    if (lane == 0) tma_prefetch_desc(&tm_o);
+    const int out_rows = a.L - a.q_off;
+    int it = 0;
+    for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); wk.valid();
+         wk.next(), ++it) {
+      const int qb = wk.qb();
+      const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
+      const int qbuf = it & 1;
+      int staged = 1;
+      if (lane == 0) staged = mbar_wait(epi_staged, it & 1, abort_flag) ? 1 : 0;
+      staged = __shfl_sync(0xffffffffu, staged, 0);
+      __syncwarp();
+      if (!staged) break;
+      const uint8_t *src = a.sep_stage ? sStage : sQ + qbuf * kQBytes;
+      const int row0 = qb * plan.Tq - a.q_off;  // out row of the block's first position
+      if (row0 >= 0) {
+        if (lane == 0) {
+          for (int c = 0; c < kChunks; ++c)
+            tma_store_4d(&tm_o, src + c * kChunkBytes, c * 64, kvh * plan.G, row0, b);
+          tma_store_commit();
+          tma_store_wait_read();
+        }
+      } else {
+        for (int i = lane; i < plan.rows * (D / 8); i += 32) {
+          const int r = i / (D / 8), u = i % (D / 8);  // tile row, 16-byte unit
+          const int orow = row0 + r / plan.G;
+          if (orow < 0 || orow >= out_rows) continue;
+          const int ch = u / 8, unit = u % 8;
+          const uint4 val = *reinterpret_cast<const uint4 *>(src + ch * kChunkBytes + r * 128 +
+                                                             ((unit ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4 *>(
+              a.out + (((size_t)b * out_rows + orow) * a.Hq + kvh * plan.G + r % plan.G) * D +
+              ch * 64 + unit * 8) = val;
+        }
+        // the buffer is next written by TMA (a Q load) or by the softmax warps
+        fence_proxy_async_smem();
+        __syncwarp();
       }
-      tma_store_wait_all();
+      if (lane == 0) mbar_arrive(a.sep_stage ? stage_free : &q_empty[qbuf]);
     }
+    if (lane == 0) tma_store_wait_all();
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------ softmax + epilogue
     // Warps 4-7 and 8-11 form two warpgroups. Warp 4 + q and warp 8 + q both

@@ -174,15 +174,18 @@ size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages, bool 
 // qb_first: query blocks below it are skipped (their rows of out are left
 // unwritten). Work items run from the last query block down, so dropping the
 // tail of the item range drops exactly those blocks.
+// q_off: k and v hold L rows, q and out only the last L - q_off of them (a
+// chunk after its staged prefix); query blocks wholly inside the first q_off
+// rows must be skipped through qb_first.
 template <int D>
 int launch_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
                    int Hkv, int w, int s, float scale, cudaStream_t stream,
-                   const DeviceInfo &dev, int qb_first = 0, float *lse = nullptr) {
+                   const DeviceInfo &dev, int qb_first = 0, float *lse = nullptr, int q_off = 0) {
   const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
   CUtensorMap tq, tk, tv, tks, tvs, to;
   int rc;
-  if ((rc = make_map_bf16_4d(&tq, q, B, L, Hq, D, plan.G, plan.Tq))) return rc;
-  if ((rc = make_map_bf16_4d(&to, out, B, L, Hq, D, plan.G, plan.Tq))) return rc;
+  if ((rc = make_map_bf16_4d(&tq, q, B, L - q_off, Hq, D, plan.G, plan.Tq))) return rc;
+  if ((rc = make_map_bf16_4d(&to, out, B, L - q_off, Hq, D, plan.G, plan.Tq))) return rc;
   if ((rc = make_map_bf16_4d(&tk, k, B, L, Hkv, D, 1, plan.n_band))) return rc;
   if ((rc = make_map_bf16_4d(&tv, v, B, L, Hkv, D, 1, plan.n_band))) return rc;
   if (plan.n_sink > 0) {
@@ -209,6 +212,7 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.Hkv = Hkv;
   a.w = w;
   a.s = s;
+  a.q_off = q_off;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.plan = plan;
   a.n_items = B * Hkv * (plan.nqb - qb_first);
@@ -395,23 +399,20 @@ int noalloc_scratch_ptr(void **out) {
 }
 
 // Device workspace of swa_prefill_chunk: the append's positions, then the
-// staged q, k, v and the prefill output over the prefix + chunk rows.
+// staged keys and values over the prefix + chunk rows.
 struct ChunkWorkspace {
-  size_t pos, qx, kx, vx, ox, total;
+  size_t pos, kx, vx, total;
 };
 
-ChunkWorkspace chunk_workspace(int B, int T, int Hq, int Hkv, int d, int w, int s,
-                               long long pos0) {
+ChunkWorkspace chunk_workspace(int B, int T, int Hkv, int d, int w, int s, long long pos0) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t Lx = (size_t)(swa::chunk_prefix_rows(pos0, w, s) + T);
-  const size_t qb = up((size_t)B * Lx * Hq * d * 2), kvb = up((size_t)B * Lx * Hkv * d * 2);
+  const size_t kvb = up((size_t)B * Lx * Hkv * d * 2);
   ChunkWorkspace c;
   c.pos = 0;
-  c.qx = up((size_t)B * sizeof(int));
-  c.kx = c.qx + qb;
+  c.kx = up((size_t)B * sizeof(int));
   c.vx = c.kx + kvb;
-  c.ox = c.vx + kvb;
-  c.total = c.ox + qb;
+  c.total = c.vx + kvb;
   return c;
 }
 
@@ -712,13 +713,18 @@ size_t swa_prefill_chunk_workspace_size(int B, int T, int Hq, int Hkv, int d, in
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || w < 1 || s < 0 || pos0 < 0 ||
       !supported_d(d))
     return 0;
-  return chunk_workspace(B, T, Hq, Hkv, d, w, s, pos0).total;
+  return chunk_workspace(B, T, Hkv, d, w, s, pos0).total;
 }
 
-int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kcache,
-                      void *vcache, void *out, int B, int T, int Hq, int Hkv, int d, int w, int s,
-                      long long pos0, float scale, void *workspace, size_t workspace_bytes,
-                      swa_stream_t stream) {
+// The chunked prefill over a ring cache (src.table == nullptr) or a paged
+// pool: stage the kept K/V rows and the chunk's, run the prefill kernel on
+// the query blocks holding chunk rows (q read and out written in place), then
+// append the chunk.
+static int prefill_chunk_impl(const void *q, const void *k_new, const void *v_new, void *kcache,
+                       void *vcache, const int *page_table, int page_size, int max_pages,
+                       int n_pages, void *out, int B, int T, int Hq, int Hkv, int d, int w, int s,
+                       long long pos0, float scale, void *workspace, size_t workspace_bytes,
+                       swa_stream_t stream) {
   if (!q || !k_new || !v_new || !kcache || !vcache || !out)
     return fail(SWA_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kcache) ||
@@ -734,51 +740,75 @@ int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void 
   if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
   if (pos0 + T > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "positions beyond int32");
   if (B > 65535) return fail(SWA_ERR_UNSUPPORTED, "B > 65535");
-  const ChunkWorkspace ws = chunk_workspace(B, T, Hq, Hkv, d, w, s, pos0);
+  const ChunkWorkspace ws = chunk_workspace(B, T, Hkv, d, w, s, pos0);
   if (!workspace || workspace_bytes < ws.total)
     return fail(SWA_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, ws.total);
   const int n_pre = (int)swa::chunk_prefix_rows(pos0, w, s);
   const int Lx = n_pre + T;
   const int Tq = 128 / (Hq / Hkv);  // query positions per prefill block
-  if ((long long)B * Hkv * swa::cdiv(Lx, 128 / (Hq / Hkv)) > 0x7FFFFFFFll)
+  if ((long long)B * Hkv * swa::cdiv(Lx, Tq) > 0x7FFFFFFFll)
     return fail(SWA_ERR_UNSUPPORTED, "too many query blocks");
   DeviceInfo dev;
   if ((rc = current_device_info(&dev))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *base = reinterpret_cast<uint8_t *>(workspace);
   int *wpos = reinterpret_cast<int *>(base + ws.pos);
-  void *qx = base + ws.qx, *kx = base + ws.kx, *vx = base + ws.vx, *ox = base + ws.ox;
+  void *kx = base + ws.kx, *vx = base + ws.vx;
 
-  // 1. stage [kept cache rows | chunk] contiguously
+  // 1. stage the keys and values [kept cache rows | chunk] contiguously
+  swa::ChunkSource src;
+  src.kcache = reinterpret_cast<const uint4 *>(kcache);
+  src.vcache = reinterpret_cast<const uint4 *>(vcache);
+  src.table = page_table;
+  src.page_size = page_size;
+  src.max_pages = max_pages;
+  src.n_pages = n_pages;
   const int threads = 256;
-  long long n = (long long)Lx * (Hq + 2 * Hkv) * (d / 8);
+  long long n = (long long)Lx * 2 * Hkv * (d / 8);
   if (n < B) n = B;
-  long long blocks = (n + threads - 1) / threads;
+  const long long blocks = (n + threads - 1) / threads;
   if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "chunk too large");
   cudaError_t e = launch_pdl(
       swa::swa_chunk_stage_kernel, dim3((unsigned)blocks, B), dim3(threads), 0, st,
-      reinterpret_cast<const uint4 *>(q), reinterpret_cast<const uint4 *>(k_new),
-      reinterpret_cast<const uint4 *>(v_new), reinterpret_cast<const uint4 *>(kcache),
-      reinterpret_cast<const uint4 *>(vcache), reinterpret_cast<uint4 *>(qx),
-      reinterpret_cast<uint4 *>(kx), reinterpret_cast<uint4 *>(vx), wpos, B, T, Hq, Hkv, d, w, s,
-      pos0, n_pre, (n_pre / Tq) * Tq);
-  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_chunk stage launch");
-  // 2. the prefill kernel over the staged rows
-  // (query blocks made only of prefix rows are skipped)
+      reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), src,
+      reinterpret_cast<uint4 *>(kx), reinterpret_cast<uint4 *>(vx), wpos, B, T, Hkv, d, w, s,
+      pos0, n_pre);
+  if (e != cudaSuccess) return cuda_fail(e, "chunk stage launch");
+  // 2. the prefill kernel over the staged rows, reading q and writing out in
+  // place (query blocks made only of prefix rows are skipped)
   const int qb_first = n_pre / Tq;
-  rc = d == 64 ? launch_prefill<64>(qx, kx, vx, ox, B, Lx, Hq, Hkv, w, s, scale, st, dev, qb_first)
-               : launch_prefill<128>(qx, kx, vx, ox, B, Lx, Hq, Hkv, w, s, scale, st, dev, qb_first);
+  rc = d == 64 ? launch_prefill<64>(q, kx, vx, out, B, Lx, Hq, Hkv, w, s, scale, st, dev, qb_first,
+                                    nullptr, n_pre)
+               : launch_prefill<128>(q, kx, vx, out, B, Lx, Hq, Hkv, w, s, scale, st, dev,
+                                     qb_first, nullptr, n_pre);
   if (rc) return rc;
-  // 3. the chunk's rows to out
-  n = (long long)T * Hq * (d / 8);
-  blocks = (n + threads - 1) / threads;
-  e = launch_pdl(swa::swa_chunk_out_kernel, dim3((unsigned)blocks, B), dim3(threads), 0, st,
-                 reinterpret_cast<const uint4 *>(ox), reinterpret_cast<uint4 *>(out), T, Hq, d,
-                 n_pre);
-  if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_chunk output launch");
-  // 4. append the chunk (after the staging read every cache row it needs)
-  return swa_cache_append(k_new, v_new, kcache, vcache, wpos, B, T, Hkv, d, w, s, stream);
+  // 3. append the chunk (after the staging read every cache row it needs)
+  if (page_table == nullptr)
+    return swa_cache_append(k_new, v_new, kcache, vcache, wpos, B, T, Hkv, d, w, s, stream);
+  return swa_paged_append(k_new, v_new, kcache, vcache, page_table, wpos, B, T, Hkv, d, page_size,
+                          max_pages, n_pages, w, s, stream);
+}
+
+int swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kcache,
+                      void *vcache, void *out, int B, int T, int Hq, int Hkv, int d, int w, int s,
+                      long long pos0, float scale, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream) {
+  return prefill_chunk_impl(q, k_new, v_new, kcache, vcache, nullptr, 0, 0, 0, out, B, T, Hq, Hkv,
+                            d, w, s, pos0, scale, workspace, workspace_bytes, stream);
+}
+
+int swa_paged_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *kpool,
+                            void *vpool, const int *page_table, void *out, int B, int T, int Hq,
+                            int Hkv, int d, int page_size, int max_pages, int n_pages, int w,
+                            int s, long long pos0, float scale, void *workspace,
+                            size_t workspace_bytes, swa_stream_t stream) {
+  if (!page_table) return fail(SWA_ERR_INVALID_ARG, "null page table");
+  if (page_size < 1 || max_pages < 1 || n_pages < 1)
+    return fail(SWA_ERR_INVALID_ARG, "page_size, max_pages and n_pages must be >= 1");
+  return prefill_chunk_impl(q, k_new, v_new, kpool, vpool, page_table, page_size, max_pages,
+                            n_pages, out, B, T, Hq, Hkv, d, w, s, pos0, scale, workspace,
+                            workspace_bytes, stream);
 }
 
 size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s) {
@@ -923,15 +953,23 @@ int swa_page_pool_free_pages(swa_page_pool *pool) {
 
 int swa_paged_reserve(swa_page_pool *pool, int *table, int max_pages, long long pos_hi, int w,
                       int s, int page_size) {
+  return swa_paged_reserve_range(pool, table, max_pages, pos_hi, pos_hi, w, s, page_size);
+}
+
+// The pages of the union of K(p) over pos_lo <= p <= pos_hi: the sink pages
+// and those of positions pos_lo - w + 1 .. pos_hi.
+int swa_paged_reserve_range(swa_page_pool *pool, int *table, int max_pages, long long pos_lo,
+                            long long pos_hi, int w, int s, int page_size) {
   if (!pool || !table) return fail(SWA_ERR_INVALID_ARG, "null pointer");
-  if (max_pages < 1 || pos_hi < 0 || w < 1 || s < 0 || page_size < 1)
-    return fail(SWA_ERR_INVALID_ARG, "need max_pages, w, page_size >= 1 and pos_hi, s >= 0");
+  if (max_pages < 1 || pos_lo < 0 || pos_hi < pos_lo || w < 1 || s < 0 || page_size < 1)
+    return fail(SWA_ERR_INVALID_ARG,
+                "need max_pages, w, page_size >= 1, s >= 0 and 0 <= pos_lo <= pos_hi");
   const long long last = pos_hi / page_size;
   if (last >= max_pages)
     return fail(SWA_ERR_UNSUPPORTED, "position %lld is beyond the %d-page table", pos_hi,
                 max_pages);
   const long long sink_pages = ((long long)s + page_size - 1) / page_size;
-  const long long win_lo = (pos_hi - w + 1 > 0 ? pos_hi - w + 1 : 0) / page_size;
+  const long long win_lo = (pos_lo - w + 1 > 0 ? pos_lo - w + 1 : 0) / page_size;
   const long long sink_top = sink_pages < last + 1 ? sink_pages : last + 1;  // sink pages in use
   const long long keep_lo = win_lo > sink_pages ? win_lo : sink_pages;      // window pages
   std::lock_guard<std::mutex> lock(pool->mu);

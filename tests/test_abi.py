@@ -224,12 +224,14 @@ def test_prefill_chunk_rejects_bad_arguments():
 
 
 def test_prefill_chunk_workspace_size():
-    """q, k, v and out over min(pos0, s + w - 1) + T staged rows, plus the
-    append's positions: it stops growing once pos0 passes s + w - 1."""
+    """k and v over min(pos0, s + w - 1) + T staged rows (q and out are not
+    staged), plus the append's positions: it stops growing once pos0 passes
+    s + w - 1, and does not depend on Hq."""
     f = swa.swa_prefill_chunk_workspace_size
     assert f(1, 64, 8, 2, 64, 32, 4, -1) == 0
     assert f(1, 64, 8, 2, 64, 0, 4, 0) == 0
-    row = (2 * 8 + 2 * 2) * 64 * 2          # bytes of one staged row of q, out, k, v
+    row = (2 * 2) * 64 * 2                  # bytes of one staged row of k, v
+    assert f(1, 64, 8, 2, 64, 32, 4, 35) == f(1, 64, 32, 2, 64, 32, 4, 35)
     a, b = f(1, 64, 8, 2, 64, 32, 4, 0), f(1, 64, 8, 2, 64, 32, 4, 35)
     assert b - a == 35 * row
     assert f(1, 64, 8, 2, 64, 32, 4, 10_000) == f(1, 64, 8, 2, 64, 32, 4, 35)

@@ -94,3 +94,71 @@ def test_long_chunked_prefill_sampled():
                                      np.arange(L - 16, L), rng.integers(0, L, 48)]))
     ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=rows)
     compare(out[:, torch.from_numpy(rows).to(dev)].cpu(), ref, "long chunked")
+
+
+@pytest.mark.parametrize("P", [16, 64])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%d_L%d_Hq%d_Hkv%d_d%d_w%d_s%d" % c[:7])
+def test_paged_chunked_prefill(case, P):
+    """The same chunks over the paged layout: every row equals the oracle's,
+    the pages a layer holds stay bounded, and decoding eight more tokens from
+    the pages the chunks filled gives the oracle's rows."""
+    B, L, Hq, Hkv, d, w, s, chunks = case
+    extra = 8
+    q, k, v = prefill_case(B, L + extra, Hq, Hkv, d, 7300 + L + w, sink_rows=min(s, 4))
+    sc = scale_for(d)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    per_seq = -(-(L + extra) // P) + 2
+    pool = swa.PagePool(B * per_seq, Hkv, d, page_size=P)
+    cache = swa.PagedKVCache(pool, B, w, s, max_len=L + extra)
+    outs, p = [], 0
+    for T in chunks:
+        outs.append(cache.prefill_chunk(qd[:, p:p + T].contiguous(), kd[:, p:p + T].contiguous(),
+                                        vd[:, p:p + T].contiguous(), sc))
+        p += T
+        if w < L:
+            bound = -(-s // P) + -(-(w - 1 + T) // P) + 1
+            assert cache.pages_held() <= B * bound
+    dec = []
+    for t in range(L, L + extra):
+        cache.append(kd[:, t:t + 1].contiguous(), vd[:, t:t + 1].contiguous())
+        dec.append(cache.decode(qd[:, t].contiguous(), sc))
+    torch.cuda.synchronize()
+    ref, _ = oracle.prefill(q[:, :L], k[:, :L], v[:, :L], w, s, sc)
+    compare(torch.cat(outs, 1).cpu(), ref, f"paged chunked {chunks}")
+    ref, _ = oracle.prefill(q, k, v, w, s, sc, rows=np.arange(L, L + extra))
+    compare(torch.stack(dec, 1).cpu(), ref, "paged decode after chunks")
+    cache.release()
+    assert pool.free_pages() == pool.n_pages
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_chunk_writes_only_its_rows_of_out(paged):
+    """out is written in place by the prefill kernel, including the block
+    that starts inside the staged prefix (copied with plain stores): the
+    bytes around out stay untouched and every row is the oracle's."""
+    B, L, Hq, Hkv, d, w, s = 1, 420, 8, 2, 64, 200, 4   # Tq = 32 query positions per block
+    q, k, v = prefill_case(B, L, Hq, Hkv, d, 7400, sink_rows=4)
+    sc = scale_for(d)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    if paged:
+        pool = swa.PagePool(64, Hkv, d, page_size=16)
+        cache = swa.PagedKVCache(pool, B, w, s, max_len=L)
+    else:
+        cache = swa.RingCache(B, Hkv, d, w, s, device=dev)
+    outs, p = [], 0
+    # pos0 = 100 (prefix rows 0..99: 100 % 32 = 4) and pos0 = 250 (staged
+    # prefix of s + w - 1 = 203 rows: 203 % 32 = 11), then 410 (also 203)
+    for T in (100, 150, 160, 10):
+        row = Hq * d
+        guard = torch.full(((T + 64) * row,), 7.0, dtype=torch.bfloat16, device=dev)
+        out = guard[32 * row:(32 + T) * row].view(1, T, Hq, d)
+        cache.prefill_chunk(qd[:, p:p + T].contiguous(), kd[:, p:p + T].contiguous(),
+                            vd[:, p:p + T].contiguous(), sc, out=out)
+        torch.cuda.synchronize()
+        assert (guard[:32 * row] == 7.0).all() and (guard[(32 + T) * row:] == 7.0).all(), T
+        outs.append(out.clone())
+        p += T
+    ref, _ = oracle.prefill(q, k, v, w, s, sc)
+    compare(torch.cat(outs, 1).cpu(), ref, "chunk rows in place")

@@ -98,3 +98,32 @@ def test_bad_arguments():
     assert pool.release(forged) == swa.SWA_ERR_INVALID_ARG
     assert lib.swa_page_pool_create(0) is None
     assert lib.swa_page_pool_free_pages(None) == -1
+
+
+@pytest.mark.parametrize("w,s,P", [(100, 4, 16), (64, 0, 64), (7, 20, 8), (300, 2, 32)])
+def test_range_reserve_maps_the_union_of_key_pages(w, s, P):
+    """swa_paged_reserve_range(lo, hi) maps the pages of every K(p), lo <= p <=
+    hi (what a prompt chunk at lo .. hi reads and writes), releases the rest,
+    and with lo = hi is exactly swa_paged_reserve."""
+    pool, pool1 = Pool(400), Pool(400)
+    table = np.full(1200 // P + 2, -1, dtype=np.int32)
+    single = table.copy()
+    lo = 0
+    for T in [1, 37, 200, 5, 64, 128, 1, 300]:
+        hi = lo + T - 1
+        rc = lib.swa_paged_reserve_range(pool.h, table.ctypes.data_as(ctypes.c_void_p), table.size,
+                                         lo, hi, w, s, P)
+        assert rc == swa.SWA_OK, swa.swa_last_error()
+        want = set().union(*(key_pages(p, w, s, P) for p in range(lo, hi + 1)))
+        assert mapped(table) == want, (lo, hi)
+        phys = table[table >= 0]
+        assert len(set(phys.tolist())) == len(phys)
+        assert pool.free() == pool.n - len(phys)
+        rc = lib.swa_paged_reserve_range(pool1.h, single.ctypes.data_as(ctypes.c_void_p),
+                                         single.size, hi, hi, w, s, P)
+        assert rc == swa.SWA_OK and mapped(single) == key_pages(hi, w, s, P)
+        lo = hi + 1
+    assert lib.swa_paged_reserve_range(pool.h, table.ctypes.data_as(ctypes.c_void_p), table.size,
+                                       lo, lo - 1, w, s, P) == swa.SWA_ERR_INVALID_ARG
+    assert pool.release(table) == swa.SWA_OK and pool1.release(single) == swa.SWA_OK
+    assert pool.free() == pool.n and pool1.free() == pool1.n
