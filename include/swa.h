@@ -297,6 +297,17 @@ SWA_API size_t swa_cache_bytes(int B, int Hkv, int d, int w, int s);
  * plan[7] dynamic shared memory bytes per CTA */
 SWA_API int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]);
 
+/* Test aid: which prefill kernel swa_prefill, swa_prefill_lse, the chunked
+ * prefill and the key-mask aids below use, for the whole process: 0 = the
+ * library's choice for the sizes (the default; currently always kernel 1,
+ * the faster of the two on B300 at every size measured), 1 = the kernel that
+ * computes one query block per work item, 2 = the kernel that computes two
+ * consecutive query blocks per work item over one list of key tiles. Both
+ * compute the same attention. Returns the previous mode, or -1 (nothing
+ * changed) for a mode outside 0..2. Not thread-safe against concurrent
+ * prefill calls that expect a different mode. */
+SWA_API int swa_prefill_select(int mode);
+
 /* Test aid: the (query, key) pairs that the prefill kernel's tile schedule and
  * in-tile masks admit, for rows row0 .. row0 + nrows - 1 of a prompt of length
  * L, with the same tiling as swa_prefill for these sizes.

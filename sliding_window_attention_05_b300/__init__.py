@@ -96,6 +96,8 @@ _lib.swa_cache_bytes.restype = _sz
 _lib.swa_cache_bytes.argtypes = [_i, _i, _i, _i, _i]
 _lib.swa_prefill_plan.restype = _i
 _lib.swa_prefill_plan.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]
+_lib.swa_prefill_select.restype = _i
+_lib.swa_prefill_select.argtypes = [_i]
 _lib.swa_debug_keymask.restype = _i
 _lib.swa_debug_keymask.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]
 _lib.swa_keymask_host.restype = _i
@@ -624,6 +626,19 @@ class PagedKVCache:
 
 
 # ---------------------------------------------------------------- test aids
+
+PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
+
+
+def swa_prefill_select(mode: int) -> int:
+    """Test aid: which prefill kernel runs (PREFILL_AUTO: the library's choice,
+    PREFILL_SINGLE: one query block per work item, PREFILL_PAIR: two); returns
+    the previous mode."""
+    prev = int(_lib.swa_prefill_select(int(mode)))
+    if prev < 0:
+        raise ValueError(f"prefill mode {mode} is not one of 0, 1, 2")
+    return prev
+
 
 def swa_debug_keymask(L: int, Hq: int, Hkv: int, d: int, w: int, s: int, row0: int, nrows: int,
                       device=None):

@@ -535,15 +535,17 @@ __global__ void swa_keymask_kernel(PrefillPlan plan, int L, int w, int s, int ro
   if (threadIdx.x == 0) cnt = 0;
   __syncthreads();
   const int qb = t / plan.Tq;
-  const BlockTiles bt = block_tiles(plan, qb, L, w, s);
+  // a pair item starts at the even block (a whole prompt: no blocks skipped)
+  const BlockTiles bt = block_tiles(plan, plan.bpi == 2 ? (qb & ~1) : qb, L, w, s);
   int local = 0;
   for (int i = 0; i < bt.n_tiles; ++i) {
     const Tile tl = tile_at(plan, bt, i, w, s);
     // the same column ranges the prefill softmax keeps unmasked
+    const bool full = tile_full_for(tl, qb * plan.Tq, plan.Tq, w);
     const ColRanges cr = tile_ranges(tl, t, w, s);
     for (int c = threadIdx.x; c < tl.ncols; c += blockDim.x) {
       const int j = tile_key(tl, c);
-      const bool ok = tl.full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
+      const bool ok = full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
       if (ok && j >= 0 && j < L) {
         atomicOr(&row_bits[j / 32], 1u << (j % 32));
         ++local;

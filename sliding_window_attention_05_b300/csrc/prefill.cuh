@@ -57,6 +57,8 @@ struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;         // [B, Hq, L] log-sum-exp of each row's scores (natural log), or null
   int B, L, Hq, Hkv, w, s;
+  int qb_first;       // query blocks below it are not computed (pair kernel;
+                      // the single-block kernel drops them through n_items)
   int q_off;          // K/V rows before row 0 of q and out: query row t of the
                       // key/value layout is row t - q_off of q and out, which
                       // hold L - q_off rows (0 for a whole prompt)

@@ -81,10 +81,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Slow path of mbar_wait (kept out of line: it is rarely taken, and a copy at
-// every wait would crowd the instruction cache).
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                            uint64_t timeout_ns, bool abortable) {
+// Slow path of mbar_wait, inlined where it is used (kernels whose warps re-split
+// their registers with setmaxnreg cannot call out-of-line functions).
+__device__ __forceinline__ bool mbar_wait_slow_inl(uint64_t *bar, uint32_t parity,
+                                                   volatile int *abort, uint64_t timeout_ns,
+                                                   bool abortable) {
   const uint64_t t0 = global_timer_ns();
   uint32_t it = 0;
   while (true) {
@@ -101,6 +102,13 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, vola
   }
 }
 
+// Slow path of mbar_wait (kept out of line: it is rarely taken, and a copy at
+// every wait would crowd the instruction cache).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                            uint64_t timeout_ns, bool abortable) {
+  return mbar_wait_slow_inl(bar, parity, abort, timeout_ns, abortable);
+}
+
 // Wait for the phase with the given parity to complete. Gives up after
 // timeout_ns (or, when `abortable`, as soon as another role has set *abort),
 // records the error and returns false; never spins forever. Drain waits at
@@ -110,6 +118,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
                                           bool abortable = true) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort, timeout_ns, abortable);
+}
+
+// mbar_wait with its slow path inlined (same bounds and error reporting).
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                              uint64_t timeout_ns = 2000000000ull,
+                                              bool abortable = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_inl(bar, parity, abort, timeout_ns, abortable);
 }
 
 // ---------------------------------------------------------------- proxies
@@ -350,6 +366,19 @@ __device__ __forceinline__ void reg_fence16(float (&v)[16]) {
                : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
                  "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
                  "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]));
+}
+
+// Register re-split between warpgroups (all four warps of a warpgroup execute
+// the same one). .dec returns registers to the CTA's pool; .inc waits until
+// the pool (the registers the CTA was launched with) can cover the increase,
+// so the shares must add up to at most threads x registers at launch.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- math

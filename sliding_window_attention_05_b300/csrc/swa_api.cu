@@ -21,6 +21,7 @@
 #include "decode.cuh"
 #include "page_pool.h"
 #include "prefill.cuh"
+#include "prefill_pair.cuh"
 #include "sm100_ptx.cuh"
 #include "swa_index.cuh"
 
@@ -155,18 +156,55 @@ int make_map_bf16_4d(CUtensorMap *map, const void *base, int B, int L, int H, in
 
 // ------------------------------------------------------------------ prefill
 
+// Which prefill kernel runs: 0 = by the rule in use_pair_kernel, 1 = the
+// single-block kernel, 2 = the pair kernel (set by the test aid
+// swa_prefill_select).
+std::atomic<int> g_prefill_mode{0};
+
+// The pair kernel (two query blocks per work item, prefill_pair.cuh) halves
+// the key/value loads per block, but on this GPU it runs 25-40% slower than
+// the single-block kernel at every window measured (64 to 2048; its MMA
+// issue, with N = 128 tiles, is the limit), so the library runs the
+// single-block kernel unless the pair kernel is selected explicitly.
+bool use_pair_kernel(int d, int L, int Hq, int Hkv, int w, int s) {
+  (void)d;
+  (void)L;
+  (void)Hq;
+  (void)Hkv;
+  (void)w;
+  (void)s;
+  return g_prefill_mode.load(std::memory_order_relaxed) == 2;
+}
+
+int pair_tile_keys(int d) {
+  return d == 128 ? swa::PairSmem<128>::kTileKeys : swa::PairSmem<64>::kTileKeys;
+}
+
+// The tiling of the kernel swa_prefill runs for these sizes.
+swa::PrefillPlan prefill_plan_for(int d, int L, int Hq, int Hkv, int w, int s) {
+  if (use_pair_kernel(d, L, Hq, Hkv, w, s))
+    return swa::make_plan(L, Hq, Hkv, w, s, pair_tile_keys(d), 2);
+  return swa::make_plan(L, Hq, Hkv, w, s);
+}
+
 bool prefill_sep_stage(int d, const swa::PrefillPlan &plan, int max_smem) {
   return d == 64 ? swa::PrefillSmem<64>::use_sep_stage(plan, max_smem)
                  : swa::PrefillSmem<128>::use_sep_stage(plan, max_smem);
 }
 
 int prefill_stages(int d, const swa::PrefillPlan &plan, int max_smem) {
+  if (plan.bpi == 2)
+    return d == 64 ? swa::PairSmem<64>::stages(plan, max_smem)
+                   : swa::PairSmem<128>::stages(plan, max_smem);
   const bool sep = prefill_sep_stage(d, plan, max_smem);
   return d == 64 ? swa::PrefillSmem<64>::stages(plan, max_smem, sep)
                  : swa::PrefillSmem<128>::stages(plan, max_smem, sep);
 }
 
 size_t prefill_smem_bytes(int d, const swa::PrefillPlan &plan, int stages, bool sep) {
+  if (plan.bpi == 2)
+    return d == 64 ? swa::PairSmem<64>::bytes(plan, stages)
+                   : swa::PairSmem<128>::bytes(plan, stages);
   return d == 64 ? swa::PrefillSmem<64>::bytes(plan, stages, sep)
                  : swa::PrefillSmem<128>::bytes(plan, stages, sep);
 }
@@ -181,7 +219,8 @@ template <int D>
 int launch_prefill(const void *q, const void *k, const void *v, void *out, int B, int L, int Hq,
                    int Hkv, int w, int s, float scale, cudaStream_t stream,
                    const DeviceInfo &dev, int qb_first = 0, float *lse = nullptr, int q_off = 0) {
-  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  const bool pair = use_pair_kernel(D, L, Hq, Hkv, w, s);
+  const swa::PrefillPlan plan = prefill_plan_for(D, L, Hq, Hkv, w, s);
   CUtensorMap tq, tk, tv, tks, tvs, to;
   int rc;
   if ((rc = make_map_bf16_4d(&tq, q, B, L - q_off, Hq, D, plan.G, plan.Tq))) return rc;
@@ -195,12 +234,13 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
     tks = tk;
     tvs = tv;
   }
-  const bool sep_stage = prefill_sep_stage(D, plan, dev.max_smem_optin);
+  const bool sep_stage = !pair && prefill_sep_stage(D, plan, dev.max_smem_optin);
   const int stages = prefill_stages(D, plan, dev.max_smem_optin);
   if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
-  const size_t smem = swa::PrefillSmem<D>::bytes(plan, stages, sep_stage);
-  const cudaError_t attr_err = ensure_max_dynamic_smem(
-      reinterpret_cast<const void *>(swa::swa_prefill_kernel<D>), dev.max_smem_optin);
+  const size_t smem = prefill_smem_bytes(D, plan, stages, sep_stage);
+  const void *kernel = pair ? reinterpret_cast<const void *>(swa::swa_prefill_pair_kernel<D>)
+                            : reinterpret_cast<const void *>(swa::swa_prefill_kernel<D>);
+  const cudaError_t attr_err = ensure_max_dynamic_smem(kernel, dev.max_smem_optin);
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
 
   swa::PrefillArgs a;
@@ -215,13 +255,17 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   a.q_off = q_off;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.plan = plan;
-  a.n_items = B * Hkv * (plan.nqb - qb_first);
+  a.qb_first = qb_first;
+  a.n_items = B * Hkv * (pair ? swa::cdiv(plan.nqb - qb_first, 2) : plan.nqb - qb_first);
   a.stages = stages;
-  a.kv_chunk = swa::PrefillSmem<D>::chunk_bytes(plan);
+  a.kv_chunk = plan.slot_keys * 128;
   a.sep_stage = sep_stage ? 1 : 0;
   const int grid = swa::imin(a.n_items, dev.sms);
-  cudaError_t e = launch_pdl(swa::swa_prefill_kernel<D>, dim3(grid), dim3(swa::kPrefillThreads),
-                             smem, stream, tq, tk, tv, tks, tvs, to, a);
+  cudaError_t e =
+      pair ? launch_pdl(swa::swa_prefill_pair_kernel<D>, dim3(grid), dim3(swa::kPairThreads), smem,
+                        stream, tq, tk, tv, tks, tvs, to, a)
+           : launch_pdl(swa::swa_prefill_kernel<D>, dim3(grid), dim3(swa::kPrefillThreads), smem,
+                        stream, tq, tk, tv, tks, tvs, to, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "swa_prefill launch");
   return SWA_OK;
@@ -571,7 +615,7 @@ int swa_prefill_plan(int L, int Hq, int Hkv, int d, int w, int s, int plan[8]) {
   int rc = check_heads(Hq, Hkv);
   if (rc) return rc;
   if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
-  const swa::PrefillPlan p = swa::make_plan(L, Hq, Hkv, w, s);
+  const swa::PrefillPlan p = prefill_plan_for(d, L, Hq, Hkv, w, s);
   plan[0] = p.Tq;
   plan[1] = p.rows;
   plan[2] = p.n_band;
@@ -1100,7 +1144,7 @@ int swa_debug_keymask(int L, int Hq, int Hkv, int d, int w, int s, int row0, int
   if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
   DeviceInfo dev;
   if ((rc = current_device_info(&dev))) return rc;
-  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  const swa::PrefillPlan plan = prefill_plan_for(d, L, Hq, Hkv, w, s);
   swa::swa_keymask_kernel<<<nrows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       plan, L, w, s, row0, nrows, bits, counts);
   cudaError_t e = cudaGetLastError();
@@ -1117,21 +1161,24 @@ int swa_keymask_host(int L, int Hq, int Hkv, int d, int w, int s, int row0, int 
   int rc = check_heads(Hq, Hkv);
   if (rc) return rc;
   if (!supported_d(d)) return fail(SWA_ERR_UNSUPPORTED, "head dimension %d (supported: 64, 128)", d);
-  const swa::PrefillPlan plan = swa::make_plan(L, Hq, Hkv, w, s);
+  const swa::PrefillPlan plan = prefill_plan_for(d, L, Hq, Hkv, w, s);
   const int words = swa::cdiv(L, 32);
   for (int r = 0; r < nrows; ++r) {
     const int t = row0 + r;
     uint32_t *row_bits = bits + (size_t)r * words;
     for (int i = 0; i < words; ++i) row_bits[i] = 0u;
     int cnt = 0;
-    const swa::BlockTiles bt = swa::block_tiles(plan, t / plan.Tq, L, w, s);
+    const int qb = t / plan.Tq;
+    const swa::BlockTiles bt =
+        swa::block_tiles(plan, plan.bpi == 2 ? (qb & ~1) : qb, L, w, s);
     for (int i = 0; i < bt.n_tiles; ++i) {
       const swa::Tile tl = swa::tile_at(plan, bt, i, w, s);
+      const bool full = swa::tile_full_for(tl, qb * plan.Tq, plan.Tq, w);
       const swa::ColRanges cr = swa::tile_ranges(tl, t, w, s);
       for (int c = 0; c < tl.ncols; ++c) {
         const int j = swa::tile_key(tl, c);
         const bool ok =
-            tl.full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
+            full || (c >= cr.a_lo && c < cr.a_hi) || (c >= cr.b_lo && c < cr.b_hi);
         if (ok && j >= 0 && j < L) {
           row_bits[j / 32] |= 1u << (j % 32);
           ++cnt;
@@ -1156,6 +1203,11 @@ int swa_device_error(int *code, int clear) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
   }
   return SWA_OK;
+}
+
+int swa_prefill_select(int mode) {
+  if (mode < 0 || mode > 2) return -1;
+  return g_prefill_mode.exchange(mode);
 }
 
 }  // extern "C"

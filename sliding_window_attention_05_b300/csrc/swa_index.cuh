@@ -61,6 +61,8 @@ constexpr int kMaxTileKeys = 192;
 struct PrefillPlan {
   int G;          // query heads per KV head
   int Tq;         // query positions per block
+  int bpi;        // query blocks per work item (1, or 2: a pair sharing its key tiles)
+  int kmax;       // widest key tile (MMA N)
   int rows;       // Tq * G <= 128 (rows past this stay zero)
   int n_band;     // keys per band tile (multiple of 16, <= kMaxTileKeys)
   int s_box;      // keys per sink box (multiple of 16, <= 128), 0 if s == 0
@@ -87,22 +89,28 @@ SWA_HD int cdiv_band(const PrefillPlan &p, int x) {
 #endif
 }
 
-SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
+// kmax: widest key tile; bpi: query blocks per work item. A pair item
+// (bpi = 2) covers blocks qb and qb + 1, whose key ranges differ only by Tq
+// keys at either end, so one list of key tiles serves both.
+SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s, int kmax = kMaxTileKeys,
+                             int bpi = 1) {
   PrefillPlan p;
   p.G = Hq / Hkv;
   p.Tq = 128 / p.G;
+  p.bpi = bpi;
+  p.kmax = kmax;
   p.rows = p.Tq * p.G;
   p.nqb = cdiv(L, p.Tq);
-  // Band tiles: spread the steady-state span (w + Tq - 1 keys) evenly over the
-  // fewest tiles of at most kMaxTileKeys keys, rounded up to the MMA's N
+  // Band tiles: spread the steady-state span (w + bpi * Tq - 1 keys) evenly
+  // over the fewest tiles of at most kmax keys, rounded up to the MMA's N
   // granularity of 16.
-  long long span = (long long)imin(w, L) + p.Tq - 1;
+  long long span = (long long)imin(w, L) + (long long)bpi * p.Tq - 1;
   if (span > L) span = L;
   // Tile widths are kept to multiples of 32 keys so that the two softmax
-  // warps sharing a row take equal halves of every tile (and run the same
-  // code).
-  const int nt = (int)((span + kMaxTileKeys - 1) / kMaxTileKeys);
-  p.n_band = imin(kMaxTileKeys, round_up(cdiv((int)span, nt), 32));
+  // warps sharing a row (bpi = 1) take equal halves of every tile (and run
+  // the same code).
+  const int nt = (int)((span + kmax - 1) / kmax);
+  p.n_band = imin(kmax, round_up(cdiv((int)span, nt), 32));
   if (s > 0) {
     p.n_sink = cdiv(s, 128);
     p.s_box = imin(128, round_up(cdiv(s, p.n_sink), 16));
@@ -110,7 +118,7 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
     p.n_sink = 0;
     p.s_box = 0;
   }
-  p.merge = (p.n_sink == 1 && round_up(p.s_box + p.n_band, 32) <= kMaxTileKeys) ? 1 : 0;
+  p.merge = (p.n_sink == 1 && round_up(p.s_box + p.n_band, 32) <= kmax) ? 1 : 0;
   if (p.merge) p.n_band = round_up(p.s_box + p.n_band, 32) - p.s_box;
   p.inv_band = 1.0f / (float)p.n_band;
   p.steady_tiles = (p.merge ? 0 : p.n_sink) + cdiv((int)span, p.n_band);
@@ -118,7 +126,7 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s) {
   return p;
 }
 
-// The tiles one query block visits: tiles of sink boxes first (when the sinks
+// The tiles one work item visits (for a pair, both blocks' keys): tiles of sink boxes first (when the sinks
 // do not ride in the first band tile), then band tiles that cover [lo, t_last].
 struct BlockTiles {
   int t0;          // first query position of the block
@@ -132,7 +140,7 @@ struct BlockTiles {
 SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s) {
   BlockTiles b;
   b.t0 = qb * p.Tq;
-  b.t_last = imin(b.t0 + p.Tq, L) - 1;
+  b.t_last = imin(b.t0 + p.bpi * p.Tq, L) - 1;
   int lo = imax(0, b.t0 - w + 1);  // leftmost window key of any row in the block
   b.n_sink = 0;
   b.sink_first = 0;
@@ -189,8 +197,20 @@ struct Tile {
   int own_lo;
   int own_hi;
   int ncols;     // MMA N (multiple of 16, <= kMaxTileKeys)
-  bool full;     // every (row, key) pair of the tile is admitted: no mask needed
+  bool full;     // every (row, key) pair of the tile is admitted for the
+                 // item's first block: no mask needed
 };
+
+// Whether every (row, key) pair of tile t is admitted for the query rows of
+// the block t0q .. t0q + Tq - 1: all columns are owned band keys and, for every
+// row q, inside [q - w + 1, q] (the in-band interior tiles, which need no mask).
+// For a pair item, each of its two blocks asks this for itself.
+SWA_HD bool tile_full_for(const Tile &t, int t0q, int Tq, int w) {
+  const bool owned_all = t.n_sink_cols == 0 && (t.own_hi - t.own_lo) == t.ncols;
+  const bool causal_ok = t.k0 + t.ncols - 1 <= t0q;
+  const bool window_ok = t.k0 >= t0q + Tq - 1 - w + 1;
+  return owned_all && causal_ok && window_ok;
+}
 
 SWA_HD Tile tile_at(const PrefillPlan &p, const BlockTiles &b, int i, int w, int s) {
   Tile t;
@@ -211,13 +231,7 @@ SWA_HD Tile tile_at(const PrefillPlan &p, const BlockTiles &b, int i, int w, int
   t.own_hi = imin(t.k0 + p.n_band, b.t_last + 1);
   // the loaded band box is n_band keys; columns past the owned keys are masked
   t.ncols = imin(t.n_sink_cols + p.n_band, round_up(t.n_sink_cols + t.own_hi - t.own_lo, 32));
-  // Mask-free when all columns are owned band keys and, for every row t of the
-  // block (t0 .. t0+Tq-1), inside [t - w + 1, t]: the in-band interior tiles.
-  const int t_hi = b.t0 + p.Tq - 1;
-  const bool owned_all = t.n_sink_cols == 0 && (t.own_hi - t.own_lo) == t.ncols;
-  const bool causal_ok = t.k0 + t.ncols - 1 <= b.t0;
-  const bool window_ok = t.k0 >= t_hi - w + 1;
-  t.full = owned_all && causal_ok && window_ok;
+  t.full = tile_full_for(t, b.t0, p.Tq, w);
   return t;
 }
 

@@ -120,14 +120,34 @@ def test_cache_bytes_page_examples():
     assert swa.swa_cache_bytes(1, 1, 128, g["w"], g["s"]) == g["held_tokens"] * 128 * 2
 
 
-def test_prefill_plan():
+@pytest.fixture(params=[swa.PREFILL_SINGLE, swa.PREFILL_PAIR], ids=["single", "pair"])
+def prefill_mode(request):
+    """Runs a test once per prefill kernel (the plan and key-mask aids follow it)."""
+    prev = swa.swa_prefill_select(request.param)
+    yield request.param
+    swa.swa_prefill_select(prev)
+
+
+def test_prefill_select_rejects_unknown_modes():
+    assert LIB.swa_prefill_select(3) == -1 and LIB.swa_prefill_select(-1) == -1
+    with pytest.raises(ValueError):
+        swa.swa_prefill_select(7)
+
+
+def test_prefill_plan(prefill_mode):
     p = swa.swa_prefill_plan(4096, 32, 8, 128, 128, 4)
     assert p["Tq"] == 32 and p["rows"] == 128
     assert p["n_band"] % 16 == 0 and p["n_band"] <= 192
-    # the whole steady-state span (w + Tq - 1 = 159 keys) fits one band tile
-    assert p["n_band"] >= 128 + 31
     assert p["s_box"] == 16 and p["n_sink"] == 1
     assert p["stages"] >= 2
+    if prefill_mode == swa.PREFILL_SINGLE:
+        # the whole steady-state span (w + Tq - 1 = 159 keys) fits one band tile
+        assert p["n_band"] >= 128 + 31
+    else:
+        # a pair's span (w + 2 Tq - 1 = 191 keys) in two tiles of at most 128
+        # keys, the sink box riding in the first: 16 + 112 = 128 columns
+        assert p["n_band"] == 112 and 2 * p["n_band"] >= 191
+        assert p["stages"] >= 4
     p = swa.swa_prefill_plan(300, 12, 4, 64, 40, 200)
     assert p["Tq"] == 42 and p["rows"] == 126
     assert p["n_sink"] == 2 and p["s_box"] == 112
@@ -158,7 +178,7 @@ SCHEDULE_CASES = [
 
 
 @pytest.mark.parametrize("case", SCHEDULE_CASES, ids=lambda c: "L%d_Hq%d_Hkv%d_d%d_w%d_s%d" % c)
-def test_host_schedule_matches_oracle_keysets(case):
+def test_host_schedule_matches_oracle_keysets(case, prefill_mode):
     L, Hq, Hkv, d, w, s = case
     bits, counts = swa.swa_keymask_host(L, Hq, Hkv, d, w, s, 0, L)
     got = _unpack(bits, L)
@@ -168,7 +188,7 @@ def test_host_schedule_matches_oracle_keysets(case):
     assert np.array_equal(counts.numpy(), want.sum(axis=1))
 
 
-def test_host_schedule_exhaustive_small():
+def test_host_schedule_exhaustive_small(prefill_mode):
     for L in (1, 5, 31, 32, 33, 70):
         for (Hq, Hkv) in ((1, 1), (4, 1), (6, 2), (8, 1)):
             for w in (1, 2, 3, 16, 17, 33, 64, 100):
@@ -179,13 +199,14 @@ def test_host_schedule_exhaustive_small():
                     assert np.array_equal(counts.numpy(), want.sum(axis=1)), (L, Hq, Hkv, w, s)
 
 
-def test_schedule_skips_out_of_window_tiles():
+def test_schedule_skips_out_of_window_tiles(prefill_mode):
     """Keys multiplied per query block stay O(w + Tq + sink tile), not O(t)."""
     L, Hq, Hkv, d, w, s = 32768, 32, 8, 128, 512, 4
     p = swa.swa_prefill_plan(L, Hq, Hkv, d, w, s)
     bits, counts = swa.swa_keymask_host(L, Hq, Hkv, d, w, s, L - 64, 64)
     assert counts.numpy().max() == w + s
-    visited = p["n_band"] * -(-(w + p["Tq"] - 1) // p["n_band"]) + p["s_box"]
+    blocks = 1 if prefill_mode == swa.PREFILL_SINGLE else 2   # query blocks per item
+    visited = p["n_band"] * -(-(w + blocks * p["Tq"] - 1) // p["n_band"]) + p["s_box"]
     assert visited < 2 * (w + s)
 
 

@@ -58,7 +58,16 @@ def _run(B, L, Hq, Hkv, d, w, s, seed, sink_rows=0):
     return (dq, dk, dv), ref, lse, (q, k, v)
 
 
-def test_forward_lse_matches_oracle():
+@pytest.mark.parametrize("mode", [swa.PREFILL_AUTO, swa.PREFILL_PAIR], ids=["auto", "pair"])
+def test_forward_lse_matches_oracle(mode):
+    prev = swa.swa_prefill_select(mode)
+    try:
+        _lse_case()
+    finally:
+        swa.swa_prefill_select(prev)
+
+
+def _lse_case():
     B, L, Hq, Hkv, d, w, s = 2, 300, 8, 2, 128, 40, 4
     q, k, v = prefill_case(B, L, Hq, Hkv, d, 8100, sink_rows=4)
     sc = scale_for(d)

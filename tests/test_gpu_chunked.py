@@ -132,11 +132,21 @@ def test_paged_chunked_prefill(case, P):
     assert pool.free_pages() == pool.n_pages
 
 
+@pytest.mark.parametrize("mode", [swa.PREFILL_AUTO, swa.PREFILL_PAIR], ids=["auto", "pair"])
 @pytest.mark.parametrize("paged", [False, True])
-def test_chunk_writes_only_its_rows_of_out(paged):
+def test_chunk_writes_only_its_rows_of_out(paged, mode):
     """out is written in place by the prefill kernel, including the block
     that starts inside the staged prefix (copied with plain stores): the
-    bytes around out stay untouched and every row is the oracle's."""
+    bytes around out stay untouched and every row is the oracle's. Both
+    prefill kernels."""
+    prev = swa.swa_prefill_select(mode)
+    try:
+        _chunk_rows_in_place(paged)
+    finally:
+        swa.swa_prefill_select(prev)
+
+
+def _chunk_rows_in_place(paged):
     B, L, Hq, Hkv, d, w, s = 1, 420, 8, 2, 64, 200, 4   # Tq = 32 query positions per block
     q, k, v = prefill_case(B, L, Hq, Hkv, d, 7400, sink_rows=4)
     sc = scale_for(d)

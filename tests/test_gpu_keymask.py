@@ -11,6 +11,14 @@ from test_abi import SCHEDULE_CASES, _unpack
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=[swa.PREFILL_SINGLE, swa.PREFILL_PAIR], ids=["single", "pair"])
+def kernel(request):
+    """The device and host aids replay the tiling of the selected kernel."""
+    prev = swa.swa_prefill_select(request.param)
+    yield request.param
+    swa.swa_prefill_select(prev)
+
+
 @pytest.mark.parametrize("case", SCHEDULE_CASES, ids=lambda c: "L%d_Hq%d_Hkv%d_d%d_w%d_s%d" % c)
 def test_device_keymask_matches_oracle(case):
     L, Hq, Hkv, d, w, s = case

@@ -18,6 +18,15 @@ def _device_error_clean():
     assert swa.swa_device_error(clear=True) == 0
 
 
+@pytest.fixture(autouse=True, params=[swa.PREFILL_AUTO, swa.PREFILL_PAIR], ids=["auto", "pair"])
+def kernel(request):
+    """Every test of this module runs once with the library's kernel choice
+    and once with the two-block (pair) kernel."""
+    prev = swa.swa_prefill_select(request.param)
+    yield request.param
+    swa.swa_prefill_select(prev)
+
+
 def _run(q, k, v, w, s, scale):
     dev = torch.device("cuda")
     out = swa.swa_prefill(q.to(dev), k.to(dev), v.to(dev), w, s, scale)
