@@ -57,6 +57,26 @@ KERNEL_SOURCES = ("prefill.cuh", "swa_index.cuh", "sm100_ptx.cuh")
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "swa_prefill_b2_L32768_w512_s4.md")
 
 
+PREFILL_KERNELS = {"auto": 0, "single": 1, "pair": 2}
+KERNEL_NAMES = {"auto": "swa_prefill_kernel<128>", "single": "swa_prefill_kernel<128>",
+                "pair": "swa_prefill_pair_kernel<128>"}
+
+
+def step_config(args) -> dict:
+    """The step workload, with the prompt length --L when given (a profiling
+    aid: the default is the benchmark's L)."""
+    cfg = dict(WORKLOAD)
+    if getattr(args, "L", None):
+        cfg["L"] = int(args.L)
+        cfg["name"] = (f"long prefill SWA({cfg['w']},{cfg['s']}) B={cfg['B']} L={cfg['L']}"
+                       " + append + decode")
+    return cfg
+
+
+def select_prefill_kernel(swa, args):
+    swa.swa_prefill_select(PREFILL_KERNELS[getattr(args, "prefill_kernel", "auto")])
+
+
 def pairs_per_head(L: int, w: int, s: int) -> int:
     """sum over t < L of |K(t)| = min(t+1, w) + min(s, max(0, t-w+1))."""
     t = np.arange(L, dtype=np.int64)
@@ -361,10 +381,12 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     stream = torch.cuda.Stream(device)
-    cfg = WORKLOAD
+    cfg = step_config(args)
+    select_prefill_kernel(swa, args)
     peaks = load_peaks()
+    default_run = cfg["L"] == WORKLOAD["L"] and args.prefill_kernel != "pair"
 
-    # one input set: 1.34 GB of q, k, v, far larger than the 126 MB L2
+    # one input set: 1.34 GB of q, k, v (at the default L), far larger than the 126 MB L2
     host = make_step_inputs(cfg, 1, device, seed_offset=1000 * rank)[0]
     st = GpuStep(swa, cfg, host, device)
     with torch.cuda.stream(stream):
@@ -410,11 +432,12 @@ def run_gpu(args):
         with ClockSampler(local) as clk_loop:
             pre_ms, pre_reps = replay_for(st.graph_prefill, stream, args.loop_seconds, 1)
         tf = prefill_flops(cfg) / (pre_ms * 1e-3) / 1e12
-        traffic, traffic_src = recorded_traffic()
+        traffic, traffic_src = recorded_traffic() if default_run else (
+            None, "the recorded capture is of the default L and kernel")
         roofline = dict(
             bound="tensor", achieved=round(tf, 1), peak=peaks["bf16_tflops"], unit="TFLOP/s",
             frac=round(tf / peaks["bf16_tflops"], 4), traffic=traffic,
-            kernel="swa_prefill_kernel<128>", us_per_launch=round(pre_ms * 1e3, 2),
+            kernel=KERNEL_NAMES[args.prefill_kernel], us_per_launch=round(pre_ms * 1e3, 2),
             launches_timed=pre_reps, peak_source=peaks["source"] + " (burst)",
             peak_sustained=peaks["bf16_tflops_sustained"],
             frac_sustained=(round(tf / peaks["bf16_tflops_sustained"], 4)
@@ -446,6 +469,7 @@ def run_gpu(args):
                        "global_batch": cfg["B"] * world, "seq_len": cfg["L"],
                        "parallelism": f"replicas x{world}",
                        "step": "prefill + append(prompt) + append_decode(pos=L)",
+                       "prefill_kernel": args.prefill_kernel,
                        "l2": f"inputs larger than L2 ({prefill_bytes(cfg) / 1e9:.2f} GB of "
                              f"q, k, v, out per step); CUDA graph per step half"},
             "roofline": roofline,
@@ -719,6 +743,7 @@ def run_other(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
+    select_prefill_kernel(swa, args)
     fn = {"window-sweep": bench_window_sweep, "hybrid": bench_hybrid,
           "decode-positions": bench_decode_positions, "chunked": bench_chunked,
           "paged-decode": bench_paged_decode, "backward": bench_backward}[args.workload]
@@ -806,7 +831,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    cfg = WORKLOAD
+    cfg = step_config(args)
     host = make_step_inputs(cfg, 1, None)[0]
     import oracle
     cores = os.cpu_count() or 1
@@ -856,6 +881,12 @@ def main(argv=None):
     ap.add_argument("--clocks-csv", default=None,
                     help="also write the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--prefill-kernel", choices=tuple(PREFILL_KERNELS), default="auto",
+                    help="prefill kernel: the library's choice (auto), one query block per "
+                    "work item (single) or two (pair)")
+    ap.add_argument("--L", type=int, default=None,
+                    help="prompt length of the step workload (default 32768; shorter prompts "
+                    "are for profiling small cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-decode", action="store_true", help="omit the batch-64 decode measurement")
     ap.add_argument("--skip-llama", action="store_true", help="omit the Llama-shaped layer loop")
