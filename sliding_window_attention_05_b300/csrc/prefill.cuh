@@ -155,18 +155,30 @@ __device__ __forceinline__ void softmax_part(uint32_t s_row, int c_first, int ma
       }
     }
   }
-  // partial row max of the raw scores, independent chains
-  constexpr int kChains = NC * 16 < 8 ? (NC * 16 > 0 ? NC * 16 : 1) : 8;
-  float mx[kChains];
+  // partial row max of the raw scores: eight independent chains, three-input
+  // max (two keys per instruction)
+  float m_part;
+  if constexpr (NC == 0) {
+    m_part = -INFINITY;
+  } else {
+    constexpr int kN = NC * 16;
+    float mx[8];
 #pragma unroll
-  for (int k = 0; k < kChains; ++k) mx[k] = NC > 0 ? x[k] : -INFINITY;
+    for (int k = 0; k < 8; ++k) mx[k] = x[k];
+    int e = 8;
 #pragma unroll
-  for (int e = kChains; e < NC * 16; ++e) mx[e % kChains] = fmaxf(mx[e % kChains], x[e]);
+    for (; e + 16 <= kN; e += 16)
 #pragma unroll
-  for (int k = 1; k < kChains; ++k) mx[0] = fmaxf(mx[0], mx[k]);
-  *my_max = mx[0];
+      for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[e + k], x[e + 8 + k]);
+#pragma unroll
+    for (; e < kN; e += 8)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[e + k]);
+    m_part = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+  }
+  *my_max = m_part;
   named_bar_sync(bar_id, 64);
-  const float m_tile = fmaxf(mx[0], *partner_max) * cl2;  // scale > 0: max commutes with it
+  const float m_tile = fmaxf(m_part, *partner_max) * cl2;  // scale > 0: max commutes with it
   const float m_new = fmaxf(m_used, m_tile);
   factor = 1.f;
   if (m_used == -INFINITY) {
@@ -177,25 +189,32 @@ __device__ __forceinline__ void softmax_part(uint32_t s_row, int c_first, int ma
     l_part *= factor;
   }
   const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-  float sum[kChains];
+  // four chains of paired sums
+  float sum[8];
 #pragma unroll
-  for (int k = 0; k < kChains; ++k) sum[k] = 0.f;
-  // P = 2^(x * scale * log2 e - m) as bf16: 16 keys -> 8 packed columns
+  for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+  // P = 2^(x * scale * log2 e - m) as bf16: 16 keys -> 8 packed columns; the
+  // scale-and-shift runs two keys per instruction (fma.rn.f32x2)
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      x[c * 16 + e] = fast_exp2(fmaf(x[c * 16 + e], cl2, -msub));
-      sum[e % kChains] += x[c * 16 + e];
+    for (int e = 0; e < 16; e += 2) {
+      float y0, y1;
+      fma2_bc(y0, y1, x[c * 16 + e], x[c * 16 + e + 1], cl2, -msub);
+      x[c * 16 + e] = fast_exp2(y0);
+      x[c * 16 + e + 1] = fast_exp2(y1);
+      const int k = (e >> 1) & 3;
+      add2(sum[2 * k], sum[2 * k + 1], x[c * 16 + e], x[c * 16 + e + 1]);
     }
     const float *p = &x[c * 16];
     tmem_st8(s_row + (c_first + c) * 8, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
              pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]), pack_bf16x2(p[8], p[9]),
              pack_bf16x2(p[10], p[11]), pack_bf16x2(p[12], p[13]), pack_bf16x2(p[14], p[15]));
   }
-#pragma unroll
-  for (int k = 1; k < kChains; ++k) sum[0] += sum[k];
-  l_part += sum[0];
+  add2(sum[0], sum[1], sum[2], sum[3]);
+  add2(sum[4], sum[5], sum[6], sum[7]);
+  add2(sum[0], sum[1], sum[4], sum[5]);
+  l_part += sum[0] + sum[1];
 }
 
 // O (+)= P V for one tile of nk (1 .. kMaxTileKeys / 16) 16-key steps. The
