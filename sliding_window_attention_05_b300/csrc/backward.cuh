@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
            wk.next(), ++it) {
         const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
-        const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+        const BlockTiles bt = block_tiles<false>(plan, wk.qb(), a.L, a.w, a.s);
         // Q and dO of the block, once the previous block's MMAs are done
         if (!mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) { ok = false; break; }
         mbar_arrive_expect_tx(q_full, (uint32_t)(2 * kChunks * 64 * plan.rows * 2));
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           tma_load_4d(sDO + c * kChunkBytes, &tm_do, q_full, c * 64, kvh * plan.G, bt.t0, b, pol_q);
         }
         for (int i = 0; i < bt.n_tiles && ok; ++i) {
-          const Tile t = tile_at(plan, bt, i, a.w, a.s);
+          const Tile t = tile_at<false>(plan, bt, i, a.w, a.s);
           const bool band = t.ncols > t.n_sink_cols;
           const uint32_t bytes =
               (uint32_t)(kChunks * 128 * (t.n_sink_cols + (band ? plan.n_band : 0)));
@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     bool ok = true;
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
          wk.next(), ++it) {
-      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const BlockTiles bt = block_tiles<false>(plan, wk.qb(), a.L, a.w, a.s);
       if (!warp_wait(q_full, it & 1)) { ok = false; break; }
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_at<false>(plan, bt, i, a.w, a.s);
         const uint32_t ks = cs;
         if (!warp_wait(&kv_full[ks], cph)) { ok = false; break; }
         consume();
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
          wk.next(), ++it) {
       const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
-      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const BlockTiles bt = block_tiles<false>(plan, wk.qb(), a.L, a.w, a.s);
       const int t = bt.t0 + r / plan.G;
       const int hq = kvh * plan.G + r % plan.G;
       const bool valid = r < plan.rows && t < a.L;
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const float lse2 = valid ? a.lse[ri] * kLog2e : INFINITY;
       const float Dr = valid ? a.D[ri] : 0.f;
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_at<false>(plan, bt, i, a.w, a.s);
         if (!warp_wait(s_full, g & 1)) { ok = false; break; }
         tc_fence_after();
         ColRanges cr{0, tl.ncols, 0, 0};

@@ -228,13 +228,17 @@ __device__ __forceinline__ void pv_group(int nk, uint32_t accumulate, uint32_t o
     umma_ts_if(o_tmem, p_tmem + kk * 8, vd + kk * 128, idesc, 1u, kk < nk ? 1u : 0u);
 }
 
-template <int D>
+// kSinkLast: the plan may carry the sink box in a block's last band tile
+// (plan.sink_last); the other instantiation compiles that case out.
+template <int D, bool kSinkLast>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     swa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_ks,
                        const __grid_constant__ CUtensorMap tm_vs,
+                       const __grid_constant__ CUtensorMap tm_kb,
+                       const __grid_constant__ CUtensorMap tm_vb,
                        const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a) {
   constexpr int kQBytes = PrefillSmem<D>::kQBytes;
   constexpr int kChunks = D / 64;
@@ -322,6 +326,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tma_prefetch_desc(&tm_ks);
         tma_prefetch_desc(&tm_vs);
       }
+      if (kSinkLast) {
+        tma_prefetch_desc(&tm_kb);
+        tma_prefetch_desc(&tm_vb);
+      }
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       uint32_t u = 0;        // K/V loads issued (two per tile)
@@ -345,22 +353,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (wk.valid()) {
         b = wk.bh() / a.Hkv;
         kvh = wk.bh() % a.Hkv;
-        bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+        bt = block_tiles<kSinkLast>(plan, wk.qb(), a.L, a.w, a.s);
       } else {
         done = true;
       }
       while (ok && (!done || have_prev)) {
         Tile tl{};
-        if (!done) tl = tile_at(plan, bt, i, a.w, a.s);
+        if (!done) tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
         for (int half = 0; half < 2; ++half) {  // 0: K of this tile, 1: V of the previous one
           if (half == 0 && done) continue;
           if (half == 1 && !have_prev) continue;
           const Tile &t = half == 0 ? tl : prev;
           const int tb = half == 0 ? b : prev_b, th = half == 0 ? kvh : prev_kvh;
-          // slot rows [0, n_sink_cols): the sink box; then the band box
+          // slot rows [0, n_sink_cols): the sink box; then the band box, which
+          // is s_box rows shorter in a last band tile that carries the sinks
+          // (with sink_last the only band tiles with sink columns)
           const bool band = t.ncols > t.n_sink_cols;
+          const bool short_band = kSinkLast && band && t.n_sink_cols > 0;
+          const int band_rows = short_band ? plan.n_band - plan.s_box : plan.n_band;
           const uint32_t tile_bytes =
-              (uint32_t)(kChunks * 128 * (t.n_sink_cols + (band ? plan.n_band : 0)));
+              (uint32_t)(kChunks * 128 * (t.n_sink_cols + (band ? band_rows : 0)));
           if (!mbar_wait(&kv_empty[slot], phase ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&kv_full[slot], tile_bytes);
           uint8_t *dst = sKV + slot * slot_bytes;
@@ -369,7 +381,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               tma_load_4d(dst + c * kv_chunk, half == 0 ? &tm_ks : &tm_vs, &kv_full[slot],
                           c * 64, th, t.sink_key0, tb, pol_kv);
             if (band)
-              tma_load_4d(dst + c * kv_chunk + t.n_sink_cols * 128, half == 0 ? &tm_k : &tm_v,
+              tma_load_4d(dst + c * kv_chunk + t.n_sink_cols * 128,
+                          short_band ? (half == 0 ? &tm_kb : &tm_vb)
+                                     : (half == 0 ? &tm_k : &tm_v),
                           &kv_full[slot], c * 64, th, t.k0, tb, pol_kv);
           }
           ++u;
@@ -397,7 +411,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           if (wk.valid()) {
             b = wk.bh() / a.Hkv;
             kvh = wk.bh() % a.Hkv;
-            bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+            bt = block_tiles<kSinkLast>(plan, wk.qb(), a.L, a.w, a.s);
           } else {
             done = true;
           }
@@ -470,12 +484,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
          wk.next(), ++it) {
-      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const BlockTiles bt = block_tiles<kSinkLast>(plan, wk.qb(), a.L, a.w, a.s);
       const int qbuf = it & 1;
       const uint64_t qd = qd0 + (uint32_t)qbuf * (uint32_t)(kQBytes >> 4);
       if (!warp_wait(&q_full[qbuf], (it >> 1) & 1)) { ok = false; break; }
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
         if (!warp_wait(&kv_full[cs], cph)) { ok = false; break; }
         tc_fence_after();
         // S_g is issued before P V_{g-1} (which needs the softmax of tile g - 1),
@@ -588,12 +602,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int row_pos = r / plan.G;      // position of this row within a block
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, plan.nqb); ok && wk.valid();
          wk.next(), ++it) {
-      const BlockTiles bt = block_tiles(plan, wk.qb(), a.L, a.w, a.s);
+      const BlockTiles bt = block_tiles<kSinkLast>(plan, wk.qb(), a.L, a.w, a.s);
       const int t = bt.t0 + row_pos;     // query position of this row
       float m_used = -INFINITY;          // running max (scaled, log2 units)
       float l_part = 0.f;                // sum over this warp's columns
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
         if (!warp_wait(&s_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t s_row = lane_addr + kTmemS0 + (g & 1) * kTmemSStride;

@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
            wk.next(), ++it) {
         const int b = wk.bh() / a.Hkv, kvh = wk.bh() % a.Hkv;
         const int qb = a.qb_first + 2 * wk.qb();
-        const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
+        const BlockTiles bt = block_tiles<false>(plan, qb, a.L, a.w, a.s);
         for (int i = 0; ok && i < bt.n_tiles; ++i) {
-          const Tile t = tile_at(plan, bt, i, a.w, a.s);
+          const Tile t = tile_at<false>(plan, bt, i, a.w, a.s);
           const bool band = t.ncols > t.n_sink_cols;
           const uint32_t tile_bytes =
               (uint32_t)(kChunks * 128 * (t.n_sink_cols + (band ? plan.n_band : 0)));
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, npairs); ok && wk.valid();
            wk.next(), ++it) {
         const int qb = a.qb_first + 2 * wk.qb();
-        const BlockTiles bt = block_tiles(plan, qb, a.L, a.w, a.s);
+        const BlockTiles bt = block_tiles<false>(plan, qb, a.L, a.w, a.s);
         const int n = bt.n_tiles;
         if (!mbar_wait_inl(&q_full[0], it & 1, abort_flag) ||
             !mbar_wait_inl(&q_full[1], it & 1, abort_flag)) {
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           break;
         }
         // S of the first tile for both query tiles
-        int cur_ncols = tile_at(plan, bt, 0, a.w, a.s).ncols;
+        int cur_ncols = tile_at<false>(plan, bt, 0, a.w, a.s).ncols;
         if (!mbar_wait_inl(&kv_full[ks], kph, abort_flag)) { ok = false; break; }
         tc_fence_after();
         issue_s(0, ks, cur_ncols);
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           uint32_t ks1 = vs, kph1 = vph; // K_{j+1} follows V_j
           advance(ks1, kph1, 1);
           const bool more = j + 1 < n;
-          const int nxt_ncols = more ? tile_at(plan, bt, j + 1, a.w, a.s).ncols : 0;
+          const int nxt_ncols = more ? tile_at<false>(plan, bt, j + 1, a.w, a.s).ncols : 0;
           if (!mbar_wait_inl(&kv_full[vs], vph, abort_flag)) { ok = false; break; }
           // A = P (TMEM, 8 columns per 16 keys), B = V (MN-major: d contiguous)
           const uint64_t vd = vd0 + vs * slot_step;
@@ -487,13 +487,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (ItemWalker wk(blockIdx.x, gridDim.x, a.n_items, BH, npairs); ok && wk.valid();
          wk.next(), ++it) {
       const int qb0 = a.qb_first + 2 * wk.qb();
-      const BlockTiles bt = block_tiles(plan, qb0, a.L, a.w, a.s);
+      const BlockTiles bt = block_tiles<false>(plan, qb0, a.L, a.w, a.s);
       const int t0q = (qb0 + h) * plan.Tq;  // first position of this query tile
       const int t = t0q + row_pos;          // query position of this row
       float m_used = -INFINITY;             // running max (scaled, log2 units)
       float l_sum = 0.f;
       for (int i = 0; i < bt.n_tiles; ++i, ++gt) {
-        const Tile tl = tile_at(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_at<false>(plan, bt, i, a.w, a.s);
         if (!warp_wait(&s_full[h], gt & 1)) { ok = false; break; }
         tc_fence_after();
         int mask = 0;

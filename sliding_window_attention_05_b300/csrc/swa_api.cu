@@ -184,7 +184,7 @@ int pair_tile_keys(int d) {
 swa::PrefillPlan prefill_plan_for(int d, int L, int Hq, int Hkv, int w, int s) {
   if (use_pair_kernel(d, L, Hq, Hkv, w, s))
     return swa::make_plan(L, Hq, Hkv, w, s, pair_tile_keys(d), 2);
-  return swa::make_plan(L, Hq, Hkv, w, s);
+  return swa::make_plan(L, Hq, Hkv, w, s, swa::kMaxTileKeys, 1, /*allow_sink_last=*/1);
 }
 
 bool prefill_sep_stage(int d, const swa::PrefillPlan &plan, int max_smem) {
@@ -234,12 +234,21 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
     tks = tk;
     tvs = tv;
   }
+  // band boxes shortened by the sink box, for a block's last band tile that
+  // carries the sinks at its end
+  CUtensorMap tkb = tk, tvb = tv;
+  if (plan.sink_last) {
+    if ((rc = make_map_bf16_4d(&tkb, k, B, L, Hkv, D, 1, plan.n_band - plan.s_box))) return rc;
+    if ((rc = make_map_bf16_4d(&tvb, v, B, L, Hkv, D, 1, plan.n_band - plan.s_box))) return rc;
+  }
   const bool sep_stage = !pair && prefill_sep_stage(D, plan, dev.max_smem_optin);
   const int stages = prefill_stages(D, plan, dev.max_smem_optin);
   if (stages < 2) return fail(SWA_ERR_UNSUPPORTED, "not enough shared memory for the pipeline");
   const size_t smem = prefill_smem_bytes(D, plan, stages, sep_stage);
-  const void *kernel = pair ? reinterpret_cast<const void *>(swa::swa_prefill_pair_kernel<D>)
-                            : reinterpret_cast<const void *>(swa::swa_prefill_kernel<D>);
+  const void *kernel =
+      pair ? reinterpret_cast<const void *>(swa::swa_prefill_pair_kernel<D>)
+           : plan.sink_last ? reinterpret_cast<const void *>(swa::swa_prefill_kernel<D, true>)
+                            : reinterpret_cast<const void *>(swa::swa_prefill_kernel<D, false>);
   const cudaError_t attr_err = ensure_max_dynamic_smem(kernel, dev.max_smem_optin);
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
 
@@ -264,8 +273,13 @@ int launch_prefill(const void *q, const void *k, const void *v, void *out, int B
   cudaError_t e =
       pair ? launch_pdl(swa::swa_prefill_pair_kernel<D>, dim3(grid), dim3(swa::kPairThreads), smem,
                         stream, tq, tk, tv, tks, tvs, to, a)
-           : launch_pdl(swa::swa_prefill_kernel<D>, dim3(grid), dim3(swa::kPrefillThreads), smem,
-                        stream, tq, tk, tv, tks, tvs, to, a);
+           : plan.sink_last
+               ? launch_pdl(swa::swa_prefill_kernel<D, true>, dim3(grid),
+                            dim3(swa::kPrefillThreads), smem, stream, tq, tk, tv, tks, tvs, tkb,
+                            tvb, to, a)
+               : launch_pdl(swa::swa_prefill_kernel<D, false>, dim3(grid),
+                            dim3(swa::kPrefillThreads), smem, stream, tq, tk, tv, tks, tvs, tkb,
+                            tvb, to, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "swa_prefill launch");
   return SWA_OK;

@@ -68,6 +68,9 @@ struct PrefillPlan {
   int s_box;      // keys per sink box (multiple of 16, <= 128), 0 if s == 0
   int n_sink;     // sink boxes, ceil(s / 128); 0 if s == 0
   int merge;      // 1: the (single) sink box rides in the first band tile
+  int sink_last;  // 1: otherwise the (single) sink box may ride in a block's
+                  // last band tile (when its owned keys fit in n_band - s_box
+                  // columns), ahead of a band box loaded s_box rows shorter
   int slot_keys;  // keys one K/V ring slot holds: the widest tile
   int steady_tiles;  // tiles a block far from the sequence start visits
   int nqb;        // query blocks per (batch, KV head)
@@ -91,9 +94,10 @@ SWA_HD int cdiv_band(const PrefillPlan &p, int x) {
 
 // kmax: widest key tile; bpi: query blocks per work item. A pair item
 // (bpi = 2) covers blocks qb and qb + 1, whose key ranges differ only by Tq
-// keys at either end, so one list of key tiles serves both.
+// keys at either end, so one list of key tiles serves both. allow_sink_last:
+// the kernel can load a shortened band box (sink_last below).
 SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s, int kmax = kMaxTileKeys,
-                             int bpi = 1) {
+                             int bpi = 1, int allow_sink_last = 0) {
   PrefillPlan p;
   p.G = Hq / Hkv;
   p.Tq = 128 / p.G;
@@ -121,22 +125,35 @@ SWA_HD PrefillPlan make_plan(int L, int Hq, int Hkv, int w, int s, int kmax = kM
   p.merge = (p.n_sink == 1 && round_up(p.s_box + p.n_band, 32) <= kmax) ? 1 : 0;
   if (p.merge) p.n_band = round_up(p.s_box + p.n_band, 32) - p.s_box;
   p.inv_band = 1.0f / (float)p.n_band;
-  p.steady_tiles = (p.merge ? 0 : p.n_sink) + cdiv((int)span, p.n_band);
+  // The sink box rides in the last band tile when that tile owns at most
+  // n_band - s_box keys in the steady state (the span's remainder): one tile
+  // fewer per block than a tile of sinks alone.
+  const int nb_steady = cdiv((int)span, p.n_band);
+  const int own_last_steady = (int)span - (nb_steady - 1) * p.n_band;
+  p.sink_last = (allow_sink_last && bpi == 1 && !p.merge && p.n_sink == 1 &&
+                 p.s_box < p.n_band && own_last_steady <= p.n_band - p.s_box)
+                    ? 1
+                    : 0;
+  p.steady_tiles = (p.merge || p.sink_last ? 0 : p.n_sink) + nb_steady;
   p.slot_keys = p.merge ? p.s_box + p.n_band : imax(p.n_band, p.s_box);
   return p;
 }
 
 // The tiles one work item visits (for a pair, both blocks' keys): tiles of sink boxes first (when the sinks
-// do not ride in the first band tile), then band tiles that cover [lo, t_last].
+// ride in neither the first nor the last band tile), then band tiles that cover [lo, t_last].
 struct BlockTiles {
   int t0;          // first query position of the block
   int t_last;      // last valid query position (< L)
   int lo;          // first key of the band part
   int n_sink;      // tiles made of sink boxes only
   int sink_first;  // 1: the first band tile also carries the sink box
+  int sink_last;   // 1: the last band tile also carries the sink box
   int n_tiles;     // all tiles
 };
 
+// kMaySinkLast = false compiles the sink_last case out (kernels whose plan
+// never sets it).
+template <bool kMaySinkLast = true>
 SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s) {
   BlockTiles b;
   b.t0 = qb * p.Tq;
@@ -144,11 +161,17 @@ SWA_HD BlockTiles block_tiles(const PrefillPlan &p, int qb, int L, int w, int s)
   int lo = imax(0, b.t0 - w + 1);  // leftmost window key of any row in the block
   b.n_sink = 0;
   b.sink_first = 0;
+  b.sink_last = 0;
   if (s > 0 && lo >= s) {          // sinks lie left of every row's window
-    if (p.merge)
+    if (p.merge) {
       b.sink_first = 1;
-    else
+    } else if (kMaySinkLast && p.sink_last &&
+               b.t_last - lo + 1 - (cdiv_band(p, b.t_last - lo + 1) - 1) * p.n_band <=
+                   p.n_band - p.s_box) {
+      b.sink_last = 1;             // the last band tile owns few enough keys
+    } else {
       b.n_sink = p.n_sink;
+    }
   } else if (s > 0) {
     lo = 0;                        // window reaches the sinks: one merged range
   }
@@ -212,6 +235,7 @@ SWA_HD bool tile_full_for(const Tile &t, int t0q, int Tq, int w) {
   return owned_all && causal_ok && window_ok;
 }
 
+template <bool kMaySinkLast = true>
 SWA_HD Tile tile_at(const PrefillPlan &p, const BlockTiles &b, int i, int w, int s) {
   Tile t;
   if (i < b.n_sink) {            // a tile of one sink box
@@ -224,7 +248,12 @@ SWA_HD Tile tile_at(const PrefillPlan &p, const BlockTiles &b, int i, int w, int
     return t;
   }
   const int bi = i - b.n_sink;
-  t.n_sink_cols = (b.sink_first && bi == 0) ? p.s_box : 0;
+  // the sink box rides in the first band tile (merge) or the last (sink_last);
+  // either way its columns come first, the band keys after them
+  t.n_sink_cols =
+      ((b.sink_first && bi == 0) || (kMaySinkLast && b.sink_last && i == b.n_tiles - 1))
+          ? p.s_box
+          : 0;
   t.sink_key0 = 0;
   t.k0 = b.lo + bi * p.n_band;
   t.own_lo = t.k0;

@@ -174,6 +174,12 @@ SCHEDULE_CASES = [
     (400, 4, 1, 64, 50, 200),
     (640, 32, 8, 128, 512, 100),
     (1, 4, 1, 64, 64, 4),
+    # the sink box rides at the end of a block's last band tile (three 192-key
+    # band tiles whose last one owns at most 192 - s_box keys)
+    (1100, 32, 8, 128, 512, 4),
+    (1500, 32, 8, 64, 470, 16),
+    (800, 1, 1, 64, 400, 10),
+    (700, 8, 2, 128, 460, 40),
 ]
 
 

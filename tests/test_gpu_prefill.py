@@ -64,6 +64,9 @@ EDGE_CASES = [
     (1, 1000, 32, 8, 128, 2048, 0), # full causal, many band tiles
     (3, 333, 2, 1, 64, 7, 1),       # tiny window, one sink
     (1, 129, 4, 1, 128, 128, 16),   # window and sinks on tile boundaries
+    (1, 1100, 32, 8, 128, 512, 4),  # sinks at the end of each block's last band tile
+    (2, 700, 8, 2, 128, 460, 40),   # the same with a 48-key sink box, ragged tail
+    (1, 800, 1, 1, 64, 400, 10),    # the same, MHA, d = 64
 ]
 
 
