@@ -12,18 +12,22 @@
 // (item = cta, cta + grid, ...); per item it visits the block's tile list
 // (swa_index.cuh): sink tile(s) first, then the band tiles.
 //
-// Warp roles (256 threads, one CTA per SM):
-//   warp 0      TMA producer: Q (double buffered) and a ring of K/V tiles
+// Warp roles (384 threads, one CTA per SM):
+//   warp 0      TMA producer: Q (double buffered) and a ring of K/V tiles, in the
+//               MMA's consumption order
 //   warp 1      TMEM owner and MMA issuer (one thread), in the order
 //                 S_g = Q K_g^T      -> TMEM buffer g % 2      (fp32)
 //                 O  += P_{g-1} V_{g-1}                        (fp32)
 //               P_{g-1} is read from TMEM (it overwrites S_{g-1} in place), so
 //               the tensor core computes S_g while the softmax warps still
 //               work on tile g-1, and the softmax never waits for a P buffer.
-//   warps 4-7   softmax + epilogue, one thread per tile row (TMEM lane):
-//               in-tile mask (edge chunks only), online softmax with lazy
-//               rescaling, P (bf16) to TMEM, O rescale in TMEM when the running
-//               max grows by more than 2^8, and at block end O / l -> bf16.
+//   warp 2      output store (TMA tensor store; plain stores for a block that
+//               starts before row 0 of out)
+//   warps 4-11  softmax + epilogue in two warpgroups; warps 4 + q and 8 + q own
+//               TMEM lanes 32q .. 32q + 31 (tile rows) and split each tile's
+//               columns: in-tile mask (edge chunks only), online softmax with
+//               lazy rescaling, P (bf16) to TMEM, O rescale in TMEM when the
+//               running max grows by more than 2^8, and at block end O / l -> bf16.
 //
 // Shared memory: Q 2 x (D/64) x 16 KB and a ring of K/V slots sized to the
 // plan's largest tile. Every operand is stored as 64-column chunks of 128-byte
