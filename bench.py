@@ -58,7 +58,8 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "swa_prefill_b2_L32768_w512_s4.
 
 
 PREFILL_KERNELS = {"auto": 0, "single": 1, "pair": 2}
-KERNEL_NAMES = {"auto": "swa_prefill_kernel<128>", "single": "swa_prefill_kernel<128>",
+# the step's prefill (SWA(512,4): the sink box rides in each block's last band tile)
+KERNEL_NAMES = {"auto": "swa_prefill_kernel<128, true>", "single": "swa_prefill_kernel<128, true>",
                 "pair": "swa_prefill_pair_kernel<128>"}
 
 
@@ -362,7 +363,7 @@ def bench_llama_layer(swa, device, stream, peaks, min_seconds=1.0):
     by = prefill_bytes(cfg)
     gbs = by / (ms * 1e-3) / 1e9
     return {"workload": cfg["name"], "B": cfg["B"], "L": cfg["L"], "w": cfg["w"], "s": cfg["s"],
-            "kernel": "swa_prefill_kernel<128>", "bound": "hbm",
+            "kernel": "swa_prefill_kernel<128, false>", "bound": "hbm",
             "us_per_launch": round(ms * 1e3, 2), "achieved": round(gbs, 1), "unit": "GB/s",
             "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
             "algorithmic_bytes": by,
