@@ -263,3 +263,51 @@ def test_prefill_chunk_workspace_size():
     assert b - a == 35 * row
     assert f(1, 64, 8, 2, 64, 32, 4, 10_000) == f(1, 64, 8, 2, 64, 32, 4, 35)
     assert a >= 64 * row
+
+
+def test_backward_and_lse_reject_bad_arguments():
+    """The prefill with lse and the backward check their arguments before any
+    device call (no GPU needed)."""
+    f = ctypes.c_float(0.125)
+    bwd = LIB.swa_prefill_backward
+    ws_need = swa.swa_prefill_backward_workspace_size(1, 64, 8, 2, 64, 4)
+    assert ws_need > 0
+
+    def call(lse=P, ws=P, nbytes=ws_need, B=1, L=64, Hq=8, Hkv=2, d=64, w=16, s=4, scale=f, q=P):
+        return bwd(q, P, P, P, P, lse, P, P, P, B, L, Hq, Hkv, d, w, s, scale, ws, nbytes, None)
+
+    assert call(q=NULL) == swa.SWA_ERR_INVALID_ARG
+    assert call(lse=NULL) == swa.SWA_ERR_INVALID_ARG
+    assert call(lse=ctypes.c_void_p(4098)) == swa.SWA_ERR_INVALID_ARG   # lse not 4-byte aligned
+    assert call(L=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(w=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(Hq=6, Hkv=4) == swa.SWA_ERR_INVALID_ARG
+    assert call(scale=ctypes.c_float(0.0)) == swa.SWA_ERR_INVALID_ARG
+    assert call(d=96) == swa.SWA_ERR_UNSUPPORTED
+    assert call(nbytes=ws_need - 1) == swa.SWA_ERR_INVALID_ARG
+    assert "workspace" in swa.swa_last_error()
+    lse = LIB.swa_prefill_lse
+    assert lse(P, P, P, P, NULL, 1, 64, 8, 2, 64, 16, 4, f, None) == swa.SWA_ERR_INVALID_ARG
+    assert lse(P, P, P, P, ctypes.c_void_p(4097), 1, 64, 8, 2, 64, 16, 4, f,
+               None) == swa.SWA_ERR_INVALID_ARG
+    assert lse(NULL, P, P, P, P, 1, 64, 8, 2, 64, 16, 4, f, None) == swa.SWA_ERR_INVALID_ARG
+    assert lse(P, P, P, P, P, 1, 64, 8, 2, 80, 16, 4, f, None) == swa.SWA_ERR_UNSUPPORTED
+
+
+def test_paged_prefill_chunk_rejects_bad_arguments():
+    f = ctypes.c_float(0.125)
+    fn = LIB.swa_paged_prefill_chunk
+    need = swa.swa_prefill_chunk_workspace_size(1, 64, 8, 2, 64, 32, 4, 100)
+
+    def call(table=P, P_=16, max_pages=64, n_pages=32, T=64, pos0=100, ws=P, nbytes=need, d=64):
+        return fn(P, P, P, P, P, table, P, 1, T, 8, 2, d, P_, max_pages, n_pages, 32, 4, pos0, f,
+                  ws, nbytes, None)
+
+    assert call(table=NULL) == swa.SWA_ERR_INVALID_ARG
+    assert call(P_=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(max_pages=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(n_pages=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(T=0) == swa.SWA_ERR_INVALID_ARG
+    assert call(pos0=-1) == swa.SWA_ERR_INVALID_ARG
+    assert call(d=96) == swa.SWA_ERR_UNSUPPORTED
+    assert call(nbytes=need - 1) == swa.SWA_ERR_INVALID_ARG

@@ -90,3 +90,20 @@ def test_fa_decode_layer_needs_max_len():
         swa.AttentionLayer(1, 4, 1, 64, 16, 4, fa_decode=True)
     with pytest.raises(ValueError, match="max_len"):
         swa.HybridStack(1, 4, 1, 64, [(16, 4), (40, 0)], fa_decode=True)
+
+
+def test_backward_rejects_shapes():
+    L = 32
+    q, k, v = _t(B, L, Hq, d), _t(B, L, Hkv, d), _t(B, L, Hkv, d)
+    out, dout = _t(B, L, Hq, d), _t(B, L, Hq, d)
+    lse = _t(B, Hq, L, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        swa.swa_prefill_backward(q, k, _t(B, L, Hkv, 2 * d), out, dout, lse, w, s)
+    with pytest.raises(ValueError):
+        swa.swa_prefill_backward(q, k, v, _t(B, L + 1, Hq, d), dout, lse, w, s)
+    with pytest.raises(ValueError):
+        swa.swa_prefill_backward(q, k, v, out, _t(B, L, Hq + 1, d), lse, w, s)
+    with pytest.raises(ValueError):
+        swa.swa_prefill_backward(q, k, v, out, dout, _t(B, L, Hq, dtype=torch.float32), w, s)
+    with pytest.raises(ValueError):
+        swa.swa_prefill_backward(q, k, v, out, dout, lse, w, s, dk=_t(B, L, Hq, d))
