@@ -66,33 +66,57 @@ struct BwdArgs {
 
 // ---------------------------------------------------------------- D = dO . O
 
-// One warp per row (b, t, hq): D[b, hq, t] = sum_c dO[b, t, hq, c] O[b, t, hq, c]
-// in fp32. The first threads also clear the sink keys' accumulators.
+// D[b, hq, t] = sum_c dO[b, t, hq, c] O[b, t, hq, c] in fp32, for every row.
+// Rows are numbered r = (b * Hq + hq) * L + t, the index of D, so the writes
+// are contiguous. D / 8 threads take one row, 16 bytes each (32 / (D / 8) rows
+// per warp pass), and every warp keeps four passes of loads in flight (a
+// grid-stride loop). The first threads also clear the sink keys' accumulators.
 template <int D>
 __global__ void swa_bwd_pre_kernel(const BwdArgs a, long long n_rows, long long n_sink) {
   grid_launch_dependents();
   grid_dependency_wait();
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  for (long long i = gtid; i < n_sink; i += (long long)gridDim.x * blockDim.x) {
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = gtid; i < n_sink; i += nthreads) {
     a.sink_dk[i] = 0.f;
     a.sink_dv[i] = 0.f;
   }
-  const long long row = gtid / 32;
+  constexpr int kTpr = D / 8;        // threads per row
+  constexpr int kRpw = 32 / kTpr;    // rows per warp pass
+  constexpr int kPasses = 4;         // passes in flight
   const int lane = threadIdx.x % 32;
-  if (row >= n_rows) return;
-  constexpr int EPL = D / 32;  // 4 or 2
-  const __nv_bfloat16 *o = a.out + row * D + lane * EPL;
-  const __nv_bfloat16 *g = a.dout + row * D + lane * EPL;
-  float acc = 0.f;
+  const int sub = lane / kTpr, c = lane % kTpr;
+  const long long warp = gtid / 32, nwarps = nthreads / 32;
+  for (long long base = warp * (kRpw * kPasses); base < n_rows;
+       base += nwarps * (kRpw * kPasses)) {
+    uint4 ov[kPasses], gv[kPasses];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+    for (int u = 0; u < kPasses; ++u) {
+      const long long r = base + u * kRpw + sub;
+      ov[u] = gv[u] = make_uint4(0, 0, 0, 0);
+      if (r < n_rows) {
+        const long long t = r % a.L, bh = r / a.L;            // bh = b * Hq + hq
+        const long long hq = bh % a.Hq, b = bh / a.Hq;
+        const long long off = ((b * a.L + t) * a.Hq + hq) * D + c * 8;
+        ov[u] = *reinterpret_cast<const uint4 *>(a.out + off);
+        gv[u] = *reinterpret_cast<const uint4 *>(a.dout + off);
+      }
+    }
 #pragma unroll
-  for (int off = 16; off >= 1; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    const long long hq = row % a.Hq;
-    const long long t = (row / a.Hq) % a.L;
-    const long long b = row / ((long long)a.Hq * a.L);
-    a.D[(b * a.Hq + hq) * a.L + t] = acc;
+    for (int u = 0; u < kPasses; ++u) {
+      const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov[u]);
+      const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(o2[e]), gf = __bfloat1622float2(g2[e]);
+        acc = fmaf(of.x, gf.x, fmaf(of.y, gf.y, acc));
+      }
+#pragma unroll
+      for (int off = kTpr / 2; off >= 1; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long r = base + u * kRpw + sub;
+      if (c == 0 && r < n_rows) a.D[r] = acc;
+    }
   }
 }
 

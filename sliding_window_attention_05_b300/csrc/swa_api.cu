@@ -526,9 +526,11 @@ int launch_backward(const void *q, const void *k, const void *v, const void *out
   // 1. D = dO . O, sink accumulators cleared
   const long long n_rows = (long long)B * L * Hq;
   const long long n_sink = (long long)B * Hkv * a.s_eff * D;
-  long long blocks = (n_rows * 32 + 255) / 256;
+  // a grid-stride kernel: 16 blocks of 256 threads per SM, fewer for small inputs
+  const long long rows_per_block = 8LL * (32 / (D / 8)) * 4;  // warps x rows per pass x passes
+  long long blocks = (n_rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 16LL * dev.sms) blocks = 16LL * dev.sms;
   if (blocks < 1) blocks = 1;
-  if (blocks > 0x7FFFFFFFll) return fail(SWA_ERR_UNSUPPORTED, "backward too large");
   cudaError_t e = launch_pdl(swa::swa_bwd_pre_kernel<D>, dim3((unsigned)blocks), dim3(256), 0,
                              stream, a, n_rows, n_sink);
   if (e != cudaSuccess) return cuda_fail(e, "swa_prefill_backward pre launch");
