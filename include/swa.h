@@ -104,7 +104,10 @@ SWA_API int swa_prefill_backward(const void *q, const void *k, const void *v, co
                                  int B, int L, int Hq, int Hkv, int d, int w, int s, float scale,
                                  void *workspace, size_t workspace_bytes, swa_stream_t stream);
 
-/* Ring-cache append: store T consecutive new tokens of every sequence.
+/* Ring-cache append: store T consecutive new tokens of every sequence (the
+ * rolling cache of the wiblog.cn long-context SWA article, section
+ * "与 KV Cache 的配合：轮转替换策略", with the s sinks of the SWA(w, s) explainer,
+ * section "工程落地与实践" item 3: 64 + 4 = 68 slots at w = 64, s = 4).
  *   k_new, v_new [B, T, Hkv, d] bf16     kcache, vcache [B, Hkv, s + w, d] bf16
  *   pos_start    DEVICE int32[B]: position of token 0 of this call, per sequence
  * Token i of sequence b has position p = pos_start[b] + i and goes to slot
@@ -147,7 +150,10 @@ SWA_API int swa_prefill_chunk(const void *q, const void *k_new, const void *v_ne
 /* Bytes of device workspace swa_decode needs for these sizes (0 if none). */
 SWA_API size_t swa_decode_workspace_size(int B, int Hq, int Hkv, int d, int w, int s);
 
-/* Decode: one new query per head attends over the ring cache.
+/* Decode: one new query per head attends over the ring cache: the x_t of the
+ * SWA(w, s) explainer (section "核心方法 / 1. 训练免费的 SWA(w, s)") for the
+ * newest position, read from the rolling cache of the wiblog.cn article
+ * (section "与 KV Cache 的配合：轮转替换策略").
  *   q   [B, Hq, d] bf16; out [B, Hq, d] bf16 (written)
  *   kcache, vcache [B, Hkv, s + w, d] bf16, already holding position pos[b]
  *   pos DEVICE int32[B]: position of the newest token of each sequence.
