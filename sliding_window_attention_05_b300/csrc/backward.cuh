@@ -155,8 +155,11 @@ struct BwdDqSmem {
   }
 };
 
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7
-// one thread per tile row. Tensor memory: S at column 0, dP at 192, dQ at 384.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-11
+// the row work: warps 4 + q and 8 + q own TMEM lanes 32q .. 32q + 31 (tile
+// rows) and split each tile's 16-key chunks (dS is elementwise given lse and
+// D, so the two need no exchange) and the dQ columns of the epilogue.
+// Tensor memory: S at column 0, dP at 192, dQ at 384.
 // Per tile g the MMA warp issues S_g = Q K_g^T and dP_g = dO V_g^T, the row
 // warps turn them into dS_g (bf16, written over S_g), then the MMA warp issues
 // dQ += dS_g K_g (A = dS from TMEM, B = K_g with d contiguous); the next tile's
@@ -187,14 +190,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t *q_full = bars + 0;     // Q and dO of the item landed
   uint64_t *q_empty = bars + 1;    // every MMA reading Q / dO of the item done
   uint64_t *s_full = bars + 2;     // S and dP of the tile computed
-  uint64_t *ds_full = bars + 3;    // dS written (4 warps)
+  uint64_t *ds_full = bars + 3;    // dS written (8 warps)
   uint64_t *dq_full = bars + 4;    // the item's last dQ product done
-  uint64_t *dq_free = bars + 5;    // dQ read out (4 warps)
+  uint64_t *dq_free = bars + 5;    // dQ read out (8 warps)
   uint64_t *mma_done = bars + 6;
   uint64_t *kv_full = bars + 8;    // [stages <= 8]
   uint64_t *kv_empty = bars + 16;  // [stages <= 8]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 24);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 25);
+  // [4] per TMEM lane quarter: both warps of the pair have read the tile's S
+  // (each warp's dS goes over S columns that may hold the partner's chunks)
+  uint64_t *pair_read = bars + 26;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const PrefillPlan &plan = a.plan;
   const int BH = a.B * a.Hkv;
@@ -203,9 +209,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(s_full, 1);
-    mbar_init(ds_full, 4);
+    mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
+    mbar_init(dq_free, 8);
+    for (int q = 0; q < 4; ++q) mbar_init(&pair_read[q], 2);
     mbar_init(mma_done, 1);
     for (int i = 0; i < stages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -349,9 +356,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_wait(mma_done, 0, abort_flag, 200000000ull, false);
     }
     __syncwarp();
-  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+  } else if (warp >= kSoftmaxWarp0) {
     // ---------------------------------------------------------- row warps
-    const int sub = warp - kSoftmaxWarp0;
+    const int sub = (warp - kSoftmaxWarp0) & 3;   // TMEM lane quarter
+    const int half = (warp - kSoftmaxWarp0) >> 2; // chunk half
     const int r = sub * 32 + lane;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(sub * 32) << 16);
     const uint32_t s_row = lane_addr, dp_row = lane_addr + kMaxTileKeys,
@@ -379,26 +387,48 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc_fence_after();
         ColRanges cr{0, tl.ncols, 0, 0};
         if (!tl.full) cr = tile_ranges(tl, t, a.w, a.s);
-        for (int c = 0; c < (tl.ncols >> 4); ++c) {
-          float x[16], y[16];
-          tmem_ld16(s_row + c * 16, x);
-          tmem_ld16(dp_row + c * 16, y);
-          tmem_wait_ld();
-          reg_fence16(x);
-          reg_fence16(y);
-          const uint32_t bits = range_bits16(c * 16, cr.a_lo, cr.a_hi) |
-                                range_bits16(c * 16, cr.b_lo, cr.b_hi);
-          float ds[16];
+        // this warp's chunks: the first half of the tile's 16-key chunks for
+        // warps 4-7, the rest for warps 8-11. dS of chunk c (bf16, 8 columns)
+        // goes over S columns 8c .. 8c + 7, which may hold a chunk the partner
+        // has not read yet: dS is kept in registers until both have read S.
+        constexpr int kMaxMine = (kMaxTileKeys / 16 + 1) / 2;
+        const int nch = tl.ncols >> 4, n0 = (nch + 1) >> 1;
+        const int c_lo = half ? n0 : 0, my_n = half ? nch - n0 : n0;
+        uint32_t pk[kMaxMine][8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p = ((bits >> e) & 1u) ? fast_exp2(fmaf(x[e], a.scale_log2, -lse2)) : 0.f;
-            ds[e] = p * (y[e] - Dr);
+        for (int k = 0; k < kMaxMine; ++k) {
+          if (k < my_n) {
+            const int c = c_lo + k;
+            float x[16], y[16];
+            tmem_ld16(s_row + c * 16, x);
+            tmem_ld16(dp_row + c * 16, y);
+            tmem_wait_ld();
+            reg_fence16(x);
+            reg_fence16(y);
+            const uint32_t bits = range_bits16(c * 16, cr.a_lo, cr.a_hi) |
+                                  range_bits16(c * 16, cr.b_lo, cr.b_hi);
+            float ds[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p =
+                  ((bits >> e) & 1u) ? fast_exp2(fmaf(x[e], a.scale_log2, -lse2)) : 0.f;
+              ds[e] = p * (y[e] - Dr);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[k][e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
           }
-          tmem_st8(s_row + c * 8, pack_bf16x2(ds[0], ds[1]), pack_bf16x2(ds[2], ds[3]),
-                   pack_bf16x2(ds[4], ds[5]), pack_bf16x2(ds[6], ds[7]),
-                   pack_bf16x2(ds[8], ds[9]), pack_bf16x2(ds[10], ds[11]),
-                   pack_bf16x2(ds[12], ds[13]), pack_bf16x2(ds[14], ds[15]));
         }
+        // both warps of the pair have read S (bounded wait, one arrival per warp)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pair_read[sub]);
+        if (!warp_wait(&pair_read[sub], g & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kMaxMine; ++k)
+          if (k < my_n)
+            tmem_st8(s_row + (c_lo + k) * 8, pk[k][0], pk[k][1], pk[k][2], pk[k][3], pk[k][4],
+                     pk[k][5], pk[k][6], pk[k][7]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -409,8 +439,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!warp_wait(dq_full, it & 1)) { ok = false; break; }
       tc_fence_after();
       __nv_bfloat16 *dst = a.dq + (((size_t)b * a.L + t) * a.Hq + hq) * D;
+      // each warp of the pair converts half of the D columns
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
+        const int c = half * (D / 32) + cc;
         float o[16];
         tmem_ld16(dq_row + c * 16, o);
         tmem_wait_ld();
