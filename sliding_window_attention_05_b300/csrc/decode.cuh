@@ -495,28 +495,90 @@ __global__ void __launch_bounds__(kDecodeThreads) swa_decode_kernel(const Decode
   }
 }
 
-// Merge the per-split partial results: one CTA per (b, hq), one thread per d.
+// Merge the per-split partial results of one (b, hq) per CTA, as the
+// log-sum-exp combine of split-KV decoding does:
+//   out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i,   M = max_i m_i,
+// over the splits i holding keys (l_i > 0). The splits' weights are computed
+// once per chunk of kCombineChunk splits into shared memory; the partial rows
+// are then summed by kCombineThreads / (D / 4) thread groups, each reading one
+// whole row as float4 columns, so many independent loads are in flight.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineChunk = 1024;
+
+__device__ __forceinline__ float block_reduce_256(float v, float *s_red, bool is_max) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float r = s_red[0];
+#pragma unroll
+  for (int i = 1; i < kCombineThreads / 32; ++i) r = is_max ? fmaxf(r, s_red[i]) : r + s_red[i];
+  __syncthreads();  // s_red may be written again
+  return r;
+}
+
 template <int D>
-__global__ void __launch_bounds__(D) swa_decode_combine_kernel(const float *__restrict__ part_o,
-                                                               const float2 *__restrict__ part_ml,
-                                                               __nv_bfloat16 *__restrict__ out,
-                                                               int splits) {
+__global__ void __launch_bounds__(kCombineThreads) swa_decode_combine_kernel(
+    const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
+    __nv_bfloat16 *__restrict__ out, int splits) {
+  constexpr int kCols = D / 4;                      // float4 columns of a row
+  constexpr int kGroups = kCombineThreads / kCols;  // rows summed side by side
+  __shared__ float s_f[kCombineChunk];
+  __shared__ float s_red[kCombineThreads / 32];
+  __shared__ float4 s_part[kGroups][kCols];
   grid_launch_dependents();
   grid_dependency_wait();
   const size_t bh = blockIdx.x;
-  const int e = threadIdx.x;
+  const float2 *ml = part_ml + bh * splits;
+  const float4 *po = reinterpret_cast<const float4 *>(part_o + bh * splits * D);
+  const int tid = threadIdx.x;
   float M = -INFINITY;
-  for (int i = 0; i < splits; ++i) M = fmaxf(M, part_ml[bh * splits + i].x);
-  float num = 0.f, den = 0.f;
-  for (int i = 0; i < splits; ++i) {
-    const float2 ml = part_ml[bh * splits + i];
-    if (ml.y > 0.f) {
-      const float f = fast_exp2(ml.x - M);
-      num += f * part_o[(bh * splits + i) * D + e];
-      den += f * ml.y;
+  for (int i = tid; i < splits; i += kCombineThreads) M = fmaxf(M, ml[i].x);
+  M = block_reduce_256(M, s_red, true);
+  const int c4 = tid % kCols, grp = tid / kCols;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int c0 = 0; c0 < splits; c0 += kCombineChunk) {
+    const int n = imin(kCombineChunk, splits - c0);
+    for (int i = tid; i < n; i += kCombineThreads) {
+      const float2 x = ml[c0 + i];
+      const float f = x.y > 0.f ? fast_exp2(x.x - M) : 0.f;
+      s_f[i] = f;
+      den = fmaf(f, x.y, den);
     }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = grp; i < n; i += kGroups) {
+      const float f = s_f[i];
+      // a split without keys is not read (its partial row carries no weight)
+      const float4 x = f != 0.f ? po[(size_t)(c0 + i) * kCols + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      acc.x = fmaf(f, x.x, acc.x);
+      acc.y = fmaf(f, x.y, acc.y);
+      acc.z = fmaf(f, x.z, acc.z);
+      acc.w = fmaf(f, x.w, acc.w);
+    }
+    __syncthreads();  // s_f is rewritten by the next chunk
   }
-  out[bh * D + e] = __float2bfloat16_rn(num / den);
+  den = block_reduce_256(den, s_red, false);
+  s_part[grp][c4] = acc;
+  __syncthreads();
+  if (tid < kCols) {
+    float4 o = s_part[0][tid];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) {
+      const float4 x = s_part[g][tid];
+      o.x += x.x;
+      o.y += x.y;
+      o.z += x.z;
+      o.w += x.w;
+    }
+    reinterpret_cast<uint2 *>(out + bh * D)[tid] =
+        make_uint2(pack_bf16x2(o.x / den, o.y / den), pack_bf16x2(o.z / den, o.w / den));
+  }
 }
 
 // ---------------------------------------------------------------- key-mask export

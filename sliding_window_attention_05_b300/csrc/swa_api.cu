@@ -363,8 +363,8 @@ cudaError_t launch_decode_t(const swa::DecodeArgs &a, int B, cudaStream_t stream
   // (a stalled test launch writes no partials, so there is nothing to combine)
   if (e != cudaSuccess || a.splits == 1 || a.stall) return e;
   const unsigned combine_ctas = (unsigned)((long long)B * a.Hq);
-  return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(combine_ctas), dim3(D), 0, stream,
-                    a.part_o, a.part_ml, a.out, a.splits);
+  return launch_pdl(swa::swa_decode_combine_kernel<D>, dim3(combine_ctas),
+                    dim3(swa::kCombineThreads), 0, stream, a.part_o, a.part_ml, a.out, a.splits);
 }
 
 template <int D, bool kPaged>
