@@ -85,6 +85,30 @@ def test_decode_workspace_sizes():
     assert swa.swa_decode_workspace_size(1, 32, 8, 128, 0, 4) == 0
 
 
+def test_decode_split_policy_invariants():
+    # The split count is visible through the workspace: B * Hq * splits rows of
+    # d fp32 partial outputs plus one (max, sum) pair. Whatever the shape, every
+    # split must fit what one decode CTA stages at once (256 slots), no split
+    # may be thinner than the 64-slot floor the policy keeps, and an unsplit
+    # cache must itself fit one CTA.
+    for B in (1, 2, 3, 8, 16, 64, 256):
+        for Hkv, G in ((1, 1), (2, 3), (8, 4), (8, 8), (4, 32)):
+            Hq = Hkv * G
+            for w, s in ((1, 0), (64, 4), (252, 4), (300, 4), (512, 4), (2048, 100),
+                         (16640, 0), (262144, 0)):
+                cap = s + w
+                for d in (64, 128):
+                    ws = swa.swa_decode_workspace_size(B, Hq, Hkv, d, w, s)
+                    if ws == 0:
+                        assert cap <= 256, (B, Hq, Hkv, d, w, s)
+                        continue
+                    row = B * Hq * (4 * d + 8)
+                    assert ws % row == 0, (B, Hq, Hkv, d, w, s, ws)
+                    splits = ws // row
+                    assert 2 <= splits <= -(-cap // 64), (B, Hq, Hkv, d, w, s, splits)
+                    assert -(-cap // splits) <= 256, (B, Hq, Hkv, d, w, s, splits)
+
+
 def test_cache_slot_matches_ring_simulation():
     for w in (1, 2, 3, 4, 7, 64, 100):
         for s in (0, 1, 4, 5, 100):
