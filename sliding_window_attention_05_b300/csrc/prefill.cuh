@@ -57,6 +57,19 @@ constexpr int kSoftmaxWarp0 = 4;                // warps 4-11: two softmax warpg
 constexpr int kMaxStages = 8;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max grows > 2^8
 
+// The order in which the three roles visit a block's tiles. The sink-last
+// kernel visits them last to first: its last tile holds the sink box and the
+// most recent keys, whose scores usually set a row's running maximum, so the
+// older band tiles visited after it seldom raise that maximum past the
+// lazy-rescale threshold. (Visited last, the sinks raised it in most warps,
+// each of which then rescaled O right before the block's last P V.) The
+// online softmax does not depend on the order.
+template <bool kSinkLast>
+__device__ __forceinline__ Tile tile_visit(const PrefillPlan &p, const BlockTiles &b, int i, int w,
+                                           int s) {
+  return tile_at<kSinkLast>(p, b, kSinkLast ? b.n_tiles - 1 - i : i, w, s);
+}
+
 struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;         // [B, Hq, L] log-sum-exp of each row's scores (natural log), or null
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       while (ok && (!done || have_prev)) {
         Tile tl{};
-        if (!done) tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
+        if (!done) tl = tile_visit<kSinkLast>(plan, bt, i, a.w, a.s);
         for (int half = 0; half < 2; ++half) {  // 0: K of this tile, 1: V of the previous one
           if (half == 0 && done) continue;
           if (half == 1 && !have_prev) continue;
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint64_t qd = qd0 + (uint32_t)qbuf * (uint32_t)(kQBytes >> 4);
       if (!warp_wait(&q_full[qbuf], (it >> 1) & 1)) { ok = false; break; }
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_visit<kSinkLast>(plan, bt, i, a.w, a.s);
         if (!warp_wait(&kv_full[cs], cph)) { ok = false; break; }
         tc_fence_after();
         // S_g is issued before P V_{g-1} (which needs the softmax of tile g - 1),
@@ -611,7 +624,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float m_used = -INFINITY;          // running max (scaled, log2 units)
       float l_part = 0.f;                // sum over this warp's columns
       for (int i = 0; i < bt.n_tiles; ++i, ++g) {
-        const Tile tl = tile_at<kSinkLast>(plan, bt, i, a.w, a.s);
+        const Tile tl = tile_visit<kSinkLast>(plan, bt, i, a.w, a.s);
         if (!warp_wait(&s_full[g & 1], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t s_row = lane_addr + kTmemS0 + (g & 1) * kTmemSStride;
